@@ -1,0 +1,204 @@
+/*
+ * pkv.h - C ABI of libpkv: batched attention over a paged KV cache with a
+ * per-element sliding-window mask, for NVIDIA GB300 (sm_103a).
+ *
+ * Semantics (what every entry point computes):
+ *   For request b, query row i and query head h, the key at logical position j of
+ *   the request's cache is visible iff
+ *       (!causal || j <= p) && (window_left < 0 || j >= p - window_left),
+ *   with p = q_start[b] + i (q_start defaults to kv_len_b - qo_len_b, so extend rows
+ *   sit after the cached prefix). window_left = W therefore admits the W+1 keys
+ *   [p-W, p] (the FlashInfer convention spelled out in AMD flashinfer PR #234, "Why
+ *   each fix" 1; the mask k_abs >= q_abs - window of sglang flashinfer_backend.py,
+ *   _build_swa_prefix_custom_mask), and any negative window_left means no window.
+ *   out = softmax(sm_scale * q K^T over the visible keys) V, and
+ *   lse = ln(sum over visible keys of exp(sm_scale * q.k)) (natural log of the
+ *   scaled logits). A row with no visible key gets out = 0 and lse = -inf.
+ *   Query head h reads KV head h / (num_qo_heads / num_kv_heads).
+ *
+ * Why the window lives in the plan: sglang PR #31501 ("Pass window_left at plan
+ * time for the SWA paged prefill wrapper") fixed wrong outputs caused by a plan
+ * made without the window and a run given one. Here window_left and causal are
+ * plan arguments only; pkv_run takes neither, so the two cannot disagree.
+ *
+ * Layouts (all contiguous, row-major, "NHD" as in flashinfer_backend.py):
+ *   q, out        : [total_q, num_qo_heads, head_dim] bf16
+ *   lse           : [total_q, num_qo_heads] fp32
+ *   k_cache/v_cache: [num_pages, page_size, num_kv_heads, head_dim] bf16
+ *   Request b owns pages kv_indices[kv_indptr[b] .. kv_indptr[b+1]); its last page
+ *   holds kv_last_page_len[b] in [1, page_size] valid slots, so
+ *   kv_len_b = (kv_indptr[b+1] - kv_indptr[b] - 1) * page_size + kv_last_page_len[b]
+ *   (0 when the request has no pages). The query rows of request b are
+ *   qo_indptr[b] .. qo_indptr[b+1].
+ *
+ * Errors: every call returns a pkv_status; nothing traps or aborts. Invalid
+ * arguments are rejected on the host before any launch (the "fail at plan() with a
+ * clear message" pattern of AMD flashinfer PR #234 and flashinfer_backend.py's
+ * plan-time asserts). pkv_last_error() gives a human-readable reason for the last
+ * failure on the calling thread. Faults the host cannot see (a page id outside
+ * [0, num_pages) in kv_indices) are recorded by the kernels in a device status
+ * word instead of being dereferenced; read it with pkv_plan_device_status().
+ *
+ * Threading and streams: a plan may be run from one host thread at a time; all
+ * launches are asynchronous on the caller's stream (a cudaStream_t passed as void*,
+ * NULL = legacy default stream). pkv_run and pkv_merge_state never synchronise;
+ * pkv_plan_create waits for its own upload and pkv_plan_device_status for the
+ * device.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* malformed argument (null, negative size, bad indptr) */
+    PKV_ERR_UNSUPPORTED = 2,   /* well-formed but not supported (head_dim, dtype, ...) */
+    PKV_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+    PKV_ERR_OOM = 4,           /* device or host allocation failed */
+    PKV_ERR_DEVICE_BOUNDS = 5, /* a kernel met a page id outside [0, num_pages) */
+    PKV_ERR_TIMEOUT = 6        /* a bounded device wait gave up */
+} pkv_status;
+
+typedef enum pkv_kind {
+    PKV_PREFILL = 0, /* ragged query rows per request (extend over a cached prefix) */
+    PKV_DECODE = 1   /* exactly one query row per request */
+} pkv_kind;
+
+typedef enum pkv_dtype {
+    PKV_BF16 = 0,
+    PKV_F32 = 1 /* merge_state values only */
+} pkv_dtype;
+
+/*
+ * Everything a plan needs to know. The fields mirror the arguments of the pages'
+ * plan calls (flashinfer_backend.py: fast_prefill_plan's _cached_module.plan
+ * arguments and call_begin_forward's begin_forward), with window_left and causal
+ * fixed here and nowhere else (sglang PR #31501).
+ */
+typedef struct pkv_plan_desc {
+    int32_t kind;                    /* pkv_kind */
+    int32_t batch_size;              /* B >= 0 */
+    const int32_t *qo_indptr;        /* HOST [B+1], non-decreasing from 0; PREFILL only
+                                        (DECODE: NULL, one row per request) */
+    const int32_t *kv_indptr;        /* HOST [B+1], non-decreasing from 0, in pages */
+    const int32_t *kv_last_page_len; /* HOST [B], each in [1, page_size] (ignored for a
+                                        request with no pages) */
+    const int32_t *q_start;          /* HOST [B] or NULL: position of each request's
+                                        first query row (NULL: kv_len - qo_len) */
+    const int32_t *kv_indices;       /* DEVICE [kv_indptr[B]] physical page ids; BORROWED:
+                                        must stay valid and unchanged until the last
+                                        pkv_run of this plan */
+    int32_t num_pages;               /* pages in k_cache / v_cache (bound for page ids) */
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;            /* divides num_qo_heads */
+    int32_t head_dim;                /* 64, 128 or 256 */
+    int32_t page_size;               /* >= 1 */
+    int32_t window_left;             /* W >= 0: keys [p-W, p]; < 0: no window */
+    int32_t causal;                  /* nonzero: keys j <= p only */
+    float sm_scale;                  /* logit scale, e.g. 1/sqrt(head_dim) */
+    int32_t fixed_split_size;        /* DECODE: KV tokens per split (> 0), or <= 0 to
+                                        let the plan choose */
+    int32_t disable_split_kv;        /* nonzero: one pass per (request, KV head) */
+    int32_t dtype;                   /* pkv_dtype of q, caches and out: PKV_BF16 */
+} pkv_plan_desc;
+
+typedef struct pkv_plan pkv_plan;
+
+/* Facts about a plan, for tests and benchmarks. */
+typedef struct pkv_plan_info {
+    int32_t kind;
+    int32_t num_work_items;    /* CTAs of the main kernel */
+    int32_t num_partials;      /* split-KV partial states (0: no merge pass) */
+    int32_t mask_mode;         /* 0 none, 1 causal, 2 causal + window, 3 window only */
+    int64_t workspace_bytes;   /* device memory owned by the plan */
+    int64_t total_q;           /* query rows */
+    int32_t kernels_per_run;   /* launches issued by one pkv_run */
+    int32_t reserved;
+} pkv_plan_info;
+
+/*
+ * pkv_plan_create: validate `desc`, decompose the batch into work items (request x
+ * KV head x query tile for PREFILL; request x KV head x KV split for DECODE), each
+ * with its KV tile range already clipped to [p_min - W, p_max], pick the mask
+ * specialisation, and upload the work list to a device workspace that the plan
+ * owns (cudaMalloc on the current device). The upload is issued on `stream` and
+ * waited for before returning, so the plan is usable from any stream; nothing is
+ * read back from the device (the schedule comes from the host arrays alone). Host
+ * arrays are copied and may be freed on return.
+ * Returns PKV_OK and sets *out, or an error with *out = NULL.
+ */
+PKV_API int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream);
+
+/*
+ * pkv_run: attention for the planned batch. q, caches and out are DEVICE bf16
+ * pointers in the layouts above (16-byte aligned); lse is a DEVICE fp32 pointer or
+ * NULL. All are borrowed for the duration of the launches. Asynchronous on
+ * `stream`; the caller orders `stream` after whatever wrote the inputs.
+ */
+PKV_API int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void *v_cache,
+            void *out, float *lse, void *stream);
+
+/*
+ * pkv_merge_state: combine two partial attention states over disjoint key sets
+ * (flashinfer_backend.py, _safe_merge_state / forward_extend's ragged + paged
+ * merge): for every (token, head) row,
+ *     s = ln(e^s_a + e^s_b),  v = (e^s_a v_a + e^s_b v_b) / e^s,
+ * where a state with s = -inf weighs nothing and two such states give v = 0,
+ * s = -inf. v_*: DEVICE [n_tokens, n_heads, head_dim] of `dtype` (PKV_BF16 or
+ * PKV_F32); s_*: DEVICE fp32 [n_tokens, n_heads]. v_out/s_out may alias v_a/s_a.
+ * No limit on n_heads (the pages' CUDA merge fails above 1024 threads per block).
+ */
+PKV_API int pkv_merge_state(const void *v_a, const float *s_a, const void *v_b, const float *s_b,
+                    void *v_out, float *s_out, int64_t n_tokens, int32_t n_heads,
+                    int32_t head_dim, int32_t dtype, void *stream);
+
+/* Free the plan's device workspace (synchronises with nothing; do not call while
+ * a run of this plan may still be executing). NULL is a no-op. */
+PKV_API int pkv_plan_destroy(pkv_plan *plan);
+
+/* Fill *info (host struct). */
+PKV_API int pkv_plan_get_info(const pkv_plan *plan, pkv_plan_info *info);
+
+/*
+ * Read and clear the plan's device status word: synchronises the device, stores
+ * PKV_OK or PKV_ERR_DEVICE_BOUNDS / PKV_ERR_TIMEOUT recorded by earlier runs in
+ * *status, and returns PKV_OK (or PKV_ERR_CUDA if the read itself failed).
+ */
+PKV_API int pkv_plan_device_status(const pkv_plan *plan, int32_t *status);
+
+/*
+ * Measurement hook: record ev_begin / ev_end (cudaEvent_t passed as void*; either
+ * may be NULL to stop recording it) on the run's stream immediately before and
+ * after the main attention kernel of every later pkv_run of this plan, so that the
+ * kernel can be timed alone (the split-KV merge pass is outside the pair).
+ */
+PKV_API int pkv_plan_set_timing_events(pkv_plan *plan, void *ev_begin, void *ev_end);
+
+/* Static name of a status code. */
+PKV_API const char *pkv_status_string(int status);
+
+/* Reason for the last failure on the calling thread ("" if none). */
+PKV_API const char *pkv_last_error(void);
+
+/* PKV_ABI_VERSION of the loaded library. */
+PKV_API int pkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

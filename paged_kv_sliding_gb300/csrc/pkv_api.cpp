@@ -1,0 +1,612 @@
+// Host side of libpkv: argument validation, the plan (work decomposition with the
+// window fixed at plan time), run dispatch and error reporting.
+//
+// The plan follows the shape of the pages' plan/run split (flashinfer_backend.py:
+// fast_prefill_plan builds the schedule from host-known qo/kv layouts with no
+// device-to-host read; call_begin_forward hands kv_indptr / kv_indices /
+// kv_last_page_len to begin_forward) with the change sglang PR #31501 asks for:
+// window_left and causal are given to the plan, and the run cannot override them.
+#include <algorithm>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <new>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "pkv_internal.h"
+
+using namespace pkv;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int status, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(e == cudaErrorMemoryAllocation ? PKV_ERR_OOM : PKV_ERR_CUDA, "%s: %s", what,
+                cudaGetErrorString(e));
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+}  // namespace
+
+struct pkv_plan {
+    pkv_plan_desc desc{};  // host pointers cleared after planning
+    int device = 0;
+    int mask_mode = kMaskNone;
+    int num_items = 0;
+    int num_partials = 0;
+    int num_merge_items = 0;
+    int64_t total_q = 0;
+    const int32_t *kv_indices = nullptr;  // borrowed device pointer
+    void *workspace = nullptr;
+    size_t workspace_bytes = 0;
+    RequestInfo *d_reqs = nullptr;
+    void *d_items = nullptr;
+    MergeItem *d_merge = nullptr;
+    float *d_partial_o = nullptr;
+    float *d_partial_lse = nullptr;
+    int32_t *d_status = nullptr;
+    cudaEvent_t ev_begin = nullptr;  // optional timing events around the main kernel
+    cudaEvent_t ev_end = nullptr;
+};
+
+namespace {
+
+struct HostRequest {
+    int64_t qo_begin, qo_len, kv_len, kv_page_begin, q_start;
+};
+
+int validate(const pkv_plan_desc *d, std::vector<HostRequest> &reqs)
+{
+    if (!d)
+        return fail(PKV_ERR_INVALID_ARG, "desc is NULL");
+    if (d->kind != PKV_PREFILL && d->kind != PKV_DECODE)
+        return fail(PKV_ERR_INVALID_ARG, "kind %d is neither PKV_PREFILL nor PKV_DECODE", d->kind);
+    if (d->batch_size < 0)
+        return fail(PKV_ERR_INVALID_ARG, "batch_size %d < 0", d->batch_size);
+    const int B = d->batch_size;
+    if (!d->kv_indptr || !d->kv_last_page_len)
+        return fail(PKV_ERR_INVALID_ARG, "kv_indptr and kv_last_page_len are required");
+    if (d->kind == PKV_PREFILL && !d->qo_indptr)
+        return fail(PKV_ERR_INVALID_ARG, "PKV_PREFILL needs qo_indptr");
+    if (d->num_qo_heads <= 0 || d->num_kv_heads <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "head counts must be positive (%d, %d)", d->num_qo_heads,
+                    d->num_kv_heads);
+    if (d->num_qo_heads % d->num_kv_heads != 0)
+        return fail(PKV_ERR_UNSUPPORTED, "num_qo_heads %d is not a multiple of num_kv_heads %d",
+                    d->num_qo_heads, d->num_kv_heads);
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256)
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", d->head_dim);
+    if (d->page_size <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "page_size %d <= 0", d->page_size);
+    if (d->num_pages < 0)
+        return fail(PKV_ERR_INVALID_ARG, "num_pages %d < 0", d->num_pages);
+    if (d->dtype != PKV_BF16)
+        return fail(PKV_ERR_UNSUPPORTED, "dtype %d: only PKV_BF16 q/kv/out are supported", d->dtype);
+    if (!(d->sm_scale == d->sm_scale) || std::isinf(d->sm_scale))
+        return fail(PKV_ERR_INVALID_ARG, "sm_scale is not finite");
+    if (d->kind == PKV_PREFILL &&
+        d->num_qo_heads / d->num_kv_heads > kPrefillRows)
+        return fail(PKV_ERR_UNSUPPORTED, "query-head group %d exceeds %d",
+                    d->num_qo_heads / d->num_kv_heads, kPrefillRows);
+    if (d->kv_indptr[0] != 0)
+        return fail(PKV_ERR_INVALID_ARG, "kv_indptr[0] = %d, expected 0", d->kv_indptr[0]);
+    if (d->kind == PKV_PREFILL && d->qo_indptr[0] != 0)
+        return fail(PKV_ERR_INVALID_ARG, "qo_indptr[0] = %d, expected 0", d->qo_indptr[0]);
+    if (B > 0 && d->kv_indptr[B] > 0 && !d->kv_indices)
+        return fail(PKV_ERR_INVALID_ARG, "kv_indices is NULL but the batch holds pages");
+    reqs.resize(B);
+    for (int b = 0; b < B; ++b) {
+        int64_t np = (int64_t)d->kv_indptr[b + 1] - d->kv_indptr[b];
+        if (np < 0)
+            return fail(PKV_ERR_INVALID_ARG, "kv_indptr decreases at request %d", b);
+        int64_t last = d->kv_last_page_len[b];
+        if (np > 0 && (last < 1 || last > d->page_size))
+            return fail(PKV_ERR_INVALID_ARG, "kv_last_page_len[%d] = %lld outside [1, %d]", b,
+                        (long long)last, d->page_size);
+        int64_t kv_len = np > 0 ? (np - 1) * d->page_size + last : 0;
+        if (kv_len > INT32_MAX / 2)
+            return fail(PKV_ERR_UNSUPPORTED, "request %d holds %lld tokens", b, (long long)kv_len);
+        int64_t qo_begin, qo_len;
+        if (d->kind == PKV_PREFILL) {
+            qo_begin = d->qo_indptr[b];
+            qo_len = (int64_t)d->qo_indptr[b + 1] - d->qo_indptr[b];
+            if (qo_len < 0)
+                return fail(PKV_ERR_INVALID_ARG, "qo_indptr decreases at request %d", b);
+        } else {
+            qo_begin = b;
+            qo_len = 1;
+        }
+        int64_t q_start = d->q_start ? (int64_t)d->q_start[b] : kv_len - qo_len;
+        if (std::llabs(q_start) > INT32_MAX / 2)
+            return fail(PKV_ERR_INVALID_ARG, "q_start[%d] out of range", b);
+        reqs[b] = {qo_begin, qo_len, kv_len, (int64_t)d->kv_indptr[b], q_start};
+    }
+    return PKV_OK;
+}
+
+// Visible key interval [lo, hi] (inclusive; empty when hi < lo) of the query
+// positions [p_min, p_max] taken together, for a request of kv_len keys.
+void visible_interval(int64_t p_min, int64_t p_max, int64_t kv_len, int window_left, bool causal,
+                      int64_t &lo, int64_t &hi)
+{
+    lo = window_left >= 0 ? std::max<int64_t>(0, p_min - window_left) : 0;
+    hi = causal ? std::min<int64_t>(kv_len - 1, p_max) : kv_len - 1;
+}
+
+// Greedy longest-first assignment of item costs to `slots` equal workers; returns
+// the finishing time of the busiest worker.
+double simulate_makespan(std::vector<double> costs, int slots)
+{
+    std::sort(costs.begin(), costs.end(), std::greater<double>());
+    std::priority_queue<double, std::vector<double>, std::greater<double>> load;
+    for (int i = 0; i < slots; ++i)
+        load.push(0.0);
+    for (double c : costs) {
+        double t = load.top();
+        load.pop();
+        load.push(t + c);
+    }
+    double mx = 0;
+    while (!load.empty()) {
+        mx = std::max(mx, load.top());
+        load.pop();
+    }
+    return mx;
+}
+
+int device_sm_count(int device)
+{
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0)
+        n = 148;
+    return n;
+}
+
+// Decode: pick the KV tokens per split. A pure function of the plan inputs and the
+// SM count: candidate split sizes are scored by a simulated makespan of the CTAs
+// (each costing its tokens plus a fixed overhead, plus the partial-state traffic
+// when split), and the smallest score wins.
+int64_t choose_decode_chunk(const std::vector<int64_t> &lens, int head_blocks, int sms,
+                            int ctas_per_sm)
+{
+    int64_t max_len = 0;
+    for (int64_t l : lens)
+        max_len = std::max(max_len, l);
+    if (max_len <= 256)
+        return std::max<int64_t>(max_len, 1);
+    const int slots = sms * ctas_per_sm;
+    const double kCtaOverhead = 48.0;   // token-row equivalents per CTA
+    const double kPartialCost = 24.0;   // token-row equivalents per partial (write + merge read)
+    int64_t best_chunk = max_len;
+    double best = 1e300;
+    for (int64_t c = 256;; c = round_up((int64_t)(c * 1.25), 64)) {
+        int64_t chunk = std::min(c, max_len);
+        std::vector<double> costs;
+        costs.reserve(lens.size() * 8);
+        double merge = 0;
+        for (int64_t l : lens) {
+            if (l <= 0) {
+                costs.push_back(kCtaOverhead);
+                continue;
+            }
+            int64_t n = (l + chunk - 1) / chunk;
+            int64_t per = round_up((l + n - 1) / n, 16);
+            for (int64_t s = 0; s < n; ++s) {
+                int64_t t = std::min(per, l - s * per);
+                if (t <= 0)
+                    break;
+                for (int h = 0; h < head_blocks; ++h)
+                    costs.push_back((double)t + kCtaOverhead + (n > 1 ? kPartialCost : 0.0));
+            }
+            if (n > 1)
+                merge += (double)n * head_blocks * kPartialCost / slots;
+        }
+        double score = simulate_makespan(costs, slots) + merge;
+        if (score < best * 0.995) {  // prefer fewer splits unless clearly better
+            best = score;
+            best_chunk = chunk;
+        }
+        if (chunk >= max_len)
+            break;
+    }
+    return best_chunk;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_status_string(int status)
+{
+    switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_OOM: return "PKV_ERR_OOM";
+    case PKV_ERR_DEVICE_BOUNDS: return "PKV_ERR_DEVICE_BOUNDS";
+    case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+    default: return "PKV_ERR_UNKNOWN";
+    }
+}
+
+const char *pkv_last_error(void) { return g_last_error.c_str(); }
+
+int pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
+{
+    g_last_error.clear();
+    if (!out)
+        return fail(PKV_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    std::vector<HostRequest> reqs;
+    int st = validate(desc, reqs);
+    if (st != PKV_OK)
+        return st;
+    const pkv_plan_desc &d = *desc;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    const int B = d.batch_size;
+    const int group = d.num_qo_heads / d.num_kv_heads;
+    const bool causal = d.causal != 0;
+    const int W = d.window_left < 0 ? -1 : d.window_left;
+
+    int device = 0;
+    cudaError_t ce = cudaGetDevice(&device);
+    if (ce != cudaSuccess)
+        return cuda_fail(ce, "cudaGetDevice");
+
+    std::vector<RequestInfo> h_reqs(B);
+    int64_t total_q = 0;
+    for (int b = 0; b < B; ++b) {
+        const HostRequest &r = reqs[b];
+        h_reqs[b] = {(int32_t)r.qo_begin, (int32_t)r.qo_len, (int32_t)r.kv_len,
+                     (int32_t)r.kv_page_begin, (int32_t)r.q_start, 0, 0, 0};
+        total_q = std::max<int64_t>(total_q, r.qo_begin + r.qo_len);
+    }
+
+    std::vector<PrefillItem> p_items;
+    std::vector<DecodeItem> d_items;
+    std::vector<MergeItem> m_items;
+    int num_partials = 0;
+    int mask_mode = causal ? (W >= 0 ? kMaskCausalWindow : kMaskCausal)
+                           : (W >= 0 ? kMaskWindow : kMaskNone);
+
+    if (d.kind == PKV_PREFILL) {
+        const int T = prefill_kv_tile(d.head_dim);
+        const int tq = std::max(1, kPrefillRows / group);
+        for (int b = 0; b < B; ++b) {
+            const HostRequest &r = reqs[b];
+            for (int64_t t0 = 0; t0 < r.qo_len; t0 += tq) {
+                int64_t nt = std::min<int64_t>(tq, r.qo_len - t0);
+                int64_t lo, hi;
+                visible_interval(r.q_start + t0, r.q_start + t0 + nt - 1, r.kv_len, W, causal, lo, hi);
+                int32_t tlo = 0, thi = 0;
+                if (hi >= lo) {
+                    tlo = (int32_t)(lo / T);
+                    thi = (int32_t)(hi / T + 1);
+                }
+                for (int hk = 0; hk < d.num_kv_heads; ++hk)
+                    p_items.push_back({b, hk, (int32_t)t0, (int32_t)nt, tlo, thi, 0, 0});
+            }
+        }
+        // Longest first, so the last wave is made of short items.
+        std::stable_sort(p_items.begin(), p_items.end(), [](const PrefillItem &a, const PrefillItem &b) {
+            return (a.kv_tile_hi - a.kv_tile_lo) > (b.kv_tile_hi - b.kv_tile_lo);
+        });
+    } else {
+        const int head_blocks = (group + kDecodeRows - 1) / kDecodeRows;
+        std::vector<int64_t> lens(B), los(B);
+        for (int b = 0; b < B; ++b) {
+            int64_t lo, hi;
+            const HostRequest &r = reqs[b];
+            visible_interval(r.q_start, r.q_start, r.kv_len, W, causal, lo, hi);
+            los[b] = lo;
+            lens[b] = std::max<int64_t>(0, hi - lo + 1);
+        }
+        int64_t chunk;
+        if (d.disable_split_kv) {
+            chunk = INT32_MAX;
+        } else if (d.fixed_split_size > 0) {
+            chunk = d.fixed_split_size;
+        } else {
+            const int ctas_per_sm = d.head_dim <= 128 ? 2 : 1;
+            chunk = choose_decode_chunk(lens, head_blocks * d.num_kv_heads,
+                                        device_sm_count(device), ctas_per_sm);
+        }
+        for (int b = 0; b < B; ++b) {
+            int64_t L = lens[b];
+            int64_t n = L > 0 ? (L + chunk - 1) / chunk : 1;
+            int64_t per = L > 0 ? (d.fixed_split_size > 0 && !d.disable_split_kv
+                                       ? chunk
+                                       : round_up((L + n - 1) / n, 16))
+                                : 0;
+            if (L > 0)
+                n = (L + per - 1) / per;
+            int32_t pbase = -1;
+            if (n > 1) {
+                pbase = num_partials;
+                num_partials += (int32_t)n;
+                m_items.push_back({(int32_t)reqs[b].qo_begin, pbase, (int32_t)n, 0});
+            }
+            for (int64_t s = 0; s < n; ++s) {
+                int64_t j0 = los[b] + s * per;
+                int64_t j1 = L > 0 ? std::min(los[b] + L, j0 + per) : j0;
+                for (int hk = 0; hk < d.num_kv_heads; ++hk)
+                    for (int h0 = 0; h0 < group; h0 += kDecodeRows)
+                        d_items.push_back({b, hk, hk * group + h0, std::min(kDecodeRows, group - h0),
+                                           (int32_t)j0, (int32_t)j1,
+                                           n > 1 ? (int32_t)(pbase + s) : -1, 0});
+            }
+        }
+        std::stable_sort(d_items.begin(), d_items.end(), [](const DecodeItem &a, const DecodeItem &b) {
+            return (a.j1 - a.j0) > (b.j1 - b.j0);
+        });
+    }
+
+    // One device workspace: requests | items | merge items | partial o | partial lse | status.
+    const size_t n_items = d.kind == PKV_PREFILL ? p_items.size() : d_items.size();
+    const size_t item_bytes = d.kind == PKV_PREFILL ? sizeof(PrefillItem) : sizeof(DecodeItem);
+    size_t off = 0;
+    auto carve = [&](size_t bytes) {
+        size_t at = off;
+        off = (size_t)round_up((int64_t)(off + bytes), 256);
+        return at;
+    };
+    const size_t o_reqs = carve(sizeof(RequestInfo) * std::max<size_t>(1, B));
+    const size_t o_items = carve(item_bytes * std::max<size_t>(1, n_items));
+    const size_t o_merge = carve(sizeof(MergeItem) * std::max<size_t>(1, m_items.size()));
+    const size_t o_po = carve(sizeof(float) * (size_t)num_partials * d.num_qo_heads * d.head_dim);
+    const size_t o_pl = carve(sizeof(float) * (size_t)num_partials * d.num_qo_heads);
+    const size_t o_status = carve(sizeof(int32_t) * 4);
+    const size_t ws_bytes = off;
+    const size_t upload_bytes = o_po;  // requests, items and merge items are uploaded
+
+    pkv_plan *plan = new (std::nothrow) pkv_plan();
+    if (!plan)
+        return fail(PKV_ERR_OOM, "host allocation of the plan failed");
+    ce = cudaMalloc(&plan->workspace, ws_bytes);
+    if (ce != cudaSuccess) {
+        delete plan;
+        return cuda_fail(ce, "cudaMalloc(plan workspace)");
+    }
+    std::vector<uint8_t> staging(upload_bytes, 0);
+    std::memcpy(staging.data() + o_reqs, h_reqs.data(), sizeof(RequestInfo) * B);
+    if (d.kind == PKV_PREFILL)
+        std::memcpy(staging.data() + o_items, p_items.data(), item_bytes * n_items);
+    else
+        std::memcpy(staging.data() + o_items, d_items.data(), item_bytes * n_items);
+    std::memcpy(staging.data() + o_merge, m_items.data(), sizeof(MergeItem) * m_items.size());
+    uint8_t *base = (uint8_t *)plan->workspace;
+    ce = cudaMemcpyAsync(base, staging.data(), upload_bytes, cudaMemcpyHostToDevice, stream);
+    if (ce == cudaSuccess)
+        ce = cudaMemsetAsync(base + o_status, 0, sizeof(int32_t) * 4, stream);
+    if (ce == cudaSuccess)
+        ce = cudaStreamSynchronize(stream);  // the staging buffer is freed on return
+    if (ce != cudaSuccess) {
+        cudaFree(plan->workspace);
+        delete plan;
+        return cuda_fail(ce, "uploading the plan");
+    }
+    plan->desc = d;
+    plan->desc.qo_indptr = plan->desc.kv_indptr = plan->desc.kv_last_page_len = nullptr;
+    plan->desc.q_start = nullptr;
+    plan->desc.window_left = W;
+    plan->device = device;
+    plan->mask_mode = mask_mode;
+    plan->num_items = (int)n_items;
+    plan->num_partials = num_partials;
+    plan->num_merge_items = (int)m_items.size();
+    plan->total_q = total_q;
+    plan->kv_indices = d.kv_indices;
+    plan->workspace_bytes = ws_bytes;
+    plan->d_reqs = (RequestInfo *)(base + o_reqs);
+    plan->d_items = base + o_items;
+    plan->d_merge = (MergeItem *)(base + o_merge);
+    plan->d_partial_o = (float *)(base + o_po);
+    plan->d_partial_lse = (float *)(base + o_pl);
+    plan->d_status = (int32_t *)(base + o_status);
+    *out = plan;
+    return PKV_OK;
+}
+
+int pkv_plan_destroy(pkv_plan *plan)
+{
+    if (!plan)
+        return PKV_OK;
+    cudaError_t ce = cudaFree(plan->workspace);
+    delete plan;
+    if (ce != cudaSuccess)
+        return cuda_fail(ce, "cudaFree(plan workspace)");
+    return PKV_OK;
+}
+
+int pkv_plan_get_info(const pkv_plan *plan, pkv_plan_info *info)
+{
+    if (!plan || !info)
+        return fail(PKV_ERR_INVALID_ARG, "plan and info are required");
+    std::memset(info, 0, sizeof *info);
+    info->kind = plan->desc.kind;
+    info->num_work_items = plan->num_items;
+    info->num_partials = plan->num_partials;
+    info->mask_mode = plan->mask_mode;
+    info->workspace_bytes = (int64_t)plan->workspace_bytes;
+    info->total_q = plan->total_q;
+    info->kernels_per_run = plan->num_items > 0 ? 1 + (plan->num_merge_items > 0 ? 1 : 0) : 0;
+    return PKV_OK;
+}
+
+int pkv_plan_set_timing_events(pkv_plan *plan, void *ev_begin, void *ev_end)
+{
+    if (!plan)
+        return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
+    plan->ev_begin = (cudaEvent_t)ev_begin;
+    plan->ev_end = (cudaEvent_t)ev_end;
+    return PKV_OK;
+}
+
+int pkv_plan_device_status(const pkv_plan *plan, int32_t *status)
+{
+    if (!plan || !status)
+        return fail(PKV_ERR_INVALID_ARG, "plan and status are required");
+    int32_t h = 0;
+    cudaError_t ce = cudaDeviceSynchronize();
+    if (ce == cudaSuccess)
+        ce = cudaMemcpy(&h, plan->d_status, sizeof h, cudaMemcpyDeviceToHost);
+    if (ce == cudaSuccess)
+        ce = cudaMemset(plan->d_status, 0, sizeof(int32_t));
+    if (ce != cudaSuccess)
+        return cuda_fail(ce, "reading the device status");
+    *status = h;
+    return PKV_OK;
+}
+
+static int page_shift_of(int page_size)
+{
+    if (page_size <= 0 || (page_size & (page_size - 1)))
+        return -1;
+    int s = 0;
+    while ((1 << s) < page_size)
+        ++s;
+    return s;
+}
+
+static bool misaligned(const void *p, uintptr_t a) { return ((uintptr_t)p) % a != 0; }
+
+int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void *v_cache, void *out,
+            float *lse, void *stream_)
+{
+    g_last_error.clear();
+    if (!plan)
+        return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
+    if (plan->total_q > 0 && (!q || !out))
+        return fail(PKV_ERR_INVALID_ARG, "q and out are required");
+    if (plan->num_items > 0 && (!k_cache || !v_cache))
+        return fail(PKV_ERR_INVALID_ARG, "k_cache and v_cache are required");
+    if (misaligned(q, 16) || misaligned(k_cache, 16) || misaligned(v_cache, 16) ||
+        misaligned(out, 16) || misaligned(lse, 4))
+        return fail(PKV_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned, lse 4-byte");
+    int cur = -1;
+    if (cudaGetDevice(&cur) == cudaSuccess && cur != plan->device)
+        return fail(PKV_ERR_INVALID_ARG, "plan was made on device %d, current device is %d",
+                    plan->device, cur);
+    if (plan->num_items == 0)
+        return PKV_OK;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    const pkv_plan_desc &d = plan->desc;
+    cudaError_t ce;
+    if (d.kind == PKV_DECODE) {
+        DecodeParams p{};
+        p.items = (const DecodeItem *)plan->d_items;
+        p.reqs = plan->d_reqs;
+        p.kv_indices = plan->kv_indices;
+        p.q = (const uint16_t *)q;
+        p.k_cache = (const uint16_t *)k_cache;
+        p.v_cache = (const uint16_t *)v_cache;
+        p.out = (uint16_t *)out;
+        p.lse = lse;
+        p.partial_o = plan->d_partial_o;
+        p.partial_lse = plan->d_partial_lse;
+        p.status = plan->d_status;
+        p.num_qo_heads = d.num_qo_heads;
+        p.num_kv_heads = d.num_kv_heads;
+        p.page_size = d.page_size;
+        p.page_shift = page_shift_of(d.page_size);
+        p.num_pages = d.num_pages;
+        p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
+        if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
+            return cuda_fail(ce, "cudaEventRecord");
+        ce = launch_decode(p, d.head_dim, plan->num_items, stream);
+        if (ce != cudaSuccess)
+            return cuda_fail(ce, "decode kernel launch");
+        if (plan->ev_end && (ce = cudaEventRecord(plan->ev_end, stream)) != cudaSuccess)
+            return cuda_fail(ce, "cudaEventRecord");
+        if (plan->num_merge_items > 0) {
+            MergePartialsParams m{};
+            m.items = plan->d_merge;
+            m.partial_o = plan->d_partial_o;
+            m.partial_lse = plan->d_partial_lse;
+            m.out = (uint16_t *)out;
+            m.lse = lse;
+            m.num_items = plan->num_merge_items;
+            m.num_qo_heads = d.num_qo_heads;
+            ce = launch_merge_partials(m, d.head_dim, stream);
+            if (ce != cudaSuccess)
+                return cuda_fail(ce, "split-KV merge launch");
+        }
+        return PKV_OK;
+    }
+    PrefillParams p{};
+    p.items = (const PrefillItem *)plan->d_items;
+    p.reqs = plan->d_reqs;
+    p.kv_indices = plan->kv_indices;
+    p.q = (const uint16_t *)q;
+    p.k_cache = (const uint16_t *)k_cache;
+    p.v_cache = (const uint16_t *)v_cache;
+    p.out = (uint16_t *)out;
+    p.lse = lse;
+    p.status = plan->d_status;
+    p.num_qo_heads = d.num_qo_heads;
+    p.num_kv_heads = d.num_kv_heads;
+    p.group = d.num_qo_heads / d.num_kv_heads;
+    p.tokens_per_tile = std::max(1, kPrefillRows / p.group);
+    p.page_size = d.page_size;
+    p.page_shift = page_shift_of(d.page_size);
+    p.num_pages = d.num_pages;
+    p.window_left = d.window_left;
+    p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
+    if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
+        return cuda_fail(ce, "cudaEventRecord");
+    ce = launch_prefill(p, d.head_dim, plan->mask_mode, plan->num_items, stream);
+    if (ce != cudaSuccess)
+        return cuda_fail(ce, "prefill kernel launch");
+    if (plan->ev_end && (ce = cudaEventRecord(plan->ev_end, stream)) != cudaSuccess)
+        return cuda_fail(ce, "cudaEventRecord");
+    return PKV_OK;
+}
+
+int pkv_merge_state(const void *v_a, const float *s_a, const void *v_b, const float *s_b, void *v_out,
+                    float *s_out, int64_t n_tokens, int32_t n_heads, int32_t head_dim, int32_t dtype,
+                    void *stream)
+{
+    g_last_error.clear();
+    if (n_tokens < 0 || n_heads < 0)
+        return fail(PKV_ERR_INVALID_ARG, "negative size");
+    if (dtype != PKV_BF16 && dtype != PKV_F32)
+        return fail(PKV_ERR_UNSUPPORTED, "merge_state dtype %d", dtype);
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", head_dim);
+    const int64_t rows = n_tokens * (int64_t)n_heads;
+    if (rows == 0)
+        return PKV_OK;
+    if (!v_a || !s_a || !v_b || !s_b || !v_out || !s_out)
+        return fail(PKV_ERR_INVALID_ARG, "null pointer");
+    if (misaligned(v_a, 16) || misaligned(v_b, 16) || misaligned(v_out, 16))
+        return fail(PKV_ERR_INVALID_ARG, "value pointers must be 16-byte aligned");
+    cudaError_t ce = launch_merge_state(v_a, s_a, v_b, s_b, v_out, s_out, rows, head_dim, dtype,
+                                        (cudaStream_t)stream);
+    if (ce != cudaSuccess)
+        return cuda_fail(ce, "merge_state launch");
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// Internal declarations shared by the host plan code and the kernels of libpkv.
+// Not part of the C ABI (include/pkv.h is).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Per-request facts the kernels need, computed once by the plan.
+struct RequestInfo {
+    int32_t qo_begin;       // first global query row (qo_indptr[b])
+    int32_t qo_len;         // query rows of the request
+    int32_t kv_len;         // valid tokens in its pages
+    int32_t kv_page_begin;  // kv_indptr[b]
+    int32_t q_start;        // position of its first query row
+    int32_t pad0, pad1, pad2;
+};
+
+// One CTA of the prefill kernel: a tile of packed query rows (query tokens x the
+// KV head's query-head group) of one request against the KV tiles
+// [kv_tile_lo, kv_tile_hi) that its positions can see.
+struct PrefillItem {
+    int32_t req;
+    int32_t kv_head;
+    int32_t tok0;        // first query token of the tile, within the request
+    int32_t ntok;        // query tokens in the tile
+    int32_t kv_tile_lo;  // first KV tile (in units of the kernel's KV tile)
+    int32_t kv_tile_hi;  // one past the last KV tile
+    int32_t pad0, pad1;
+};
+
+// One CTA of the decode kernel: up to kDecodeRows query heads of one request's
+// single row against the key range [j0, j1) of one KV head.
+struct DecodeItem {
+    int32_t req;
+    int32_t kv_head;
+    int32_t head0;    // first query head handled
+    int32_t nheads;   // query heads handled (<= kDecodeRows)
+    int32_t j0, j1;   // key range, already clipped to the visible interval
+    int32_t partial;  // -1: write out/lse directly; else partial slot of this split
+    int32_t pad;
+};
+
+// Merge of a request's split-KV partial states into its output row.
+struct MergeItem {
+    int32_t row;            // global query row
+    int32_t partial_begin;  // first partial slot
+    int32_t num_partials;   // splits to combine
+    int32_t pad;
+};
+
+constexpr int kDecodeRows = 16;   // query heads per decode CTA (one m16 MMA tile)
+constexpr int kPrefillRows = 128; // packed query rows per prefill CTA (UMMA M)
+
+enum MaskMode : int32_t { kMaskNone = 0, kMaskCausal = 1, kMaskCausalWindow = 2, kMaskWindow = 3 };
+
+struct DecodeParams {
+    const DecodeItem *items;
+    const RequestInfo *reqs;
+    const int32_t *kv_indices;
+    const uint16_t *q;
+    const uint16_t *k_cache;
+    const uint16_t *v_cache;
+    uint16_t *out;
+    float *lse;          // may be null
+    float *partial_o;    // [num_partials, num_qo_heads, head_dim]
+    float *partial_lse;  // [num_partials, num_qo_heads]
+    int32_t *status;
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;
+    int32_t page_size;
+    int32_t page_shift;  // log2(page_size) when a power of two, else -1
+    int32_t num_pages;
+    float sm_scale_log2; // sm_scale * log2(e)
+};
+
+struct MergePartialsParams {
+    const MergeItem *items;
+    const float *partial_o;
+    const float *partial_lse;
+    uint16_t *out;
+    float *lse;
+    int32_t num_items;
+    int32_t num_qo_heads;
+};
+
+struct PrefillParams {
+    const PrefillItem *items;
+    const RequestInfo *reqs;
+    const int32_t *kv_indices;
+    const uint16_t *q;
+    const uint16_t *k_cache;
+    const uint16_t *v_cache;
+    uint16_t *out;
+    float *lse;
+    int32_t *status;
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;
+    int32_t group;           // num_qo_heads / num_kv_heads
+    int32_t tokens_per_tile; // query tokens per CTA = floor(128 / group)
+    int32_t page_size;
+    int32_t page_shift;
+    int32_t num_pages;
+    int32_t window_left;
+    float sm_scale_log2;
+};
+
+// Launchers (one per kernel family); return cudaGetLastError() of the launch.
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s);
+cudaError_t launch_merge_partials(const MergePartialsParams &p, int head_dim, cudaStream_t s);
+cudaError_t launch_merge_state(const void *v_a, const float *s_a, const void *v_b,
+                               const float *s_b, void *v_out, float *s_out, int64_t rows,
+                               int head_dim, int dtype, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams &p, int head_dim, int mask_mode, int num_items,
+                           cudaStream_t s);
+
+// KV tile (tokens) of the prefill kernel for a head_dim.
+int prefill_kv_tile(int head_dim);
+
+}  // namespace pkv

@@ -1,0 +1,272 @@
+"""Python binding of libpkv (the C ABI in include/pkv.h) through ctypes.
+
+Argument marshalling only: every step of the attention runs in libpkv's CUDA
+kernels. PyTorch provides device memory and the current stream. Importing this
+module does not need a GPU; loading the library does not either, but running it
+does, and there is no CPU path: if libpkv.so is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = 1
+PKV_ERR_UNSUPPORTED = 2
+PKV_ERR_CUDA = 3
+PKV_ERR_OOM = 4
+PKV_ERR_DEVICE_BOUNDS = 5
+PKV_ERR_TIMEOUT = 6
+
+PKV_PREFILL = 0
+PKV_DECODE = 1
+PKV_BF16 = 0
+PKV_F32 = 1
+
+EXPORTED = ("pkv_plan_create", "pkv_run", "pkv_merge_state", "pkv_plan_destroy",
+            "pkv_plan_get_info", "pkv_plan_device_status", "pkv_status_string",
+            "pkv_last_error", "pkv_abi_version", "pkv_plan_set_timing_events")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} [{status}]")
+        self.status = status
+
+
+class PlanDesc(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int32),
+        ("batch_size", ctypes.c_int32),
+        ("qo_indptr", ctypes.c_void_p),
+        ("kv_indptr", ctypes.c_void_p),
+        ("kv_last_page_len", ctypes.c_void_p),
+        ("q_start", ctypes.c_void_p),
+        ("kv_indices", ctypes.c_void_p),
+        ("num_pages", ctypes.c_int32),
+        ("num_qo_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("window_left", ctypes.c_int32),
+        ("causal", ctypes.c_int32),
+        ("sm_scale", ctypes.c_float),
+        ("fixed_split_size", ctypes.c_int32),
+        ("disable_split_kv", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int32),
+        ("num_work_items", ctypes.c_int32),
+        ("num_partials", ctypes.c_int32),
+        ("mask_mode", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_int64),
+        ("total_q", ctypes.c_int64),
+        ("kernels_per_run", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: Optional[str] = None):
+    """Load libpkv.so (built by paged_kv_sliding_gb300.build); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libpkv.so not found at {path}: build it with "
+                "`python -m paged_kv_sliding_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        lib.pkv_plan_create.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(PlanDesc), vp]
+        lib.pkv_plan_create.restype = ctypes.c_int
+        lib.pkv_run.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        lib.pkv_run.restype = ctypes.c_int
+        lib.pkv_merge_state.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp]
+        lib.pkv_merge_state.restype = ctypes.c_int
+        lib.pkv_plan_destroy.argtypes = [vp]
+        lib.pkv_plan_destroy.restype = ctypes.c_int
+        lib.pkv_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+        lib.pkv_plan_get_info.restype = ctypes.c_int
+        lib.pkv_plan_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+        lib.pkv_plan_device_status.restype = ctypes.c_int
+        lib.pkv_status_string.argtypes = [ctypes.c_int]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_last_error.argtypes = []
+        lib.pkv_last_error.restype = ctypes.c_char_p
+        lib.pkv_plan_set_timing_events.argtypes = [vp, vp, vp]
+        lib.pkv_plan_set_timing_events.restype = ctypes.c_int
+        lib.pkv_abi_version.argtypes = []
+        lib.pkv_abi_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str):
+    if status != PKV_OK:
+        lib = load_library()
+        msg = lib.pkv_last_error().decode() or lib.pkv_status_string(status).decode()
+        raise PkvError(status, f"{what}: {msg}")
+
+
+def _stream_handle(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _host_i32(a):
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class Plan:
+    """A plan: the batch layout, head shape, window and causal mode, fixed once.
+
+    kv_indices is a device int32 tensor borrowed by the plan (kept alive here).
+    Host index arrays are copied by the library.
+    """
+
+    def __init__(self, *, kind: str, kv_indptr, kv_indices: torch.Tensor, kv_last_page_len,
+                 num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+                 num_pages: int, window_left: int = -1, causal: bool = True,
+                 sm_scale: Optional[float] = None, qo_indptr=None, q_start=None,
+                 fixed_split_size: int = -1, disable_split_kv: bool = False, stream=None):
+        self._lib = load_library()
+        self._handle = ctypes.c_void_p()
+        self.kind = kind
+        kv_indptr = _host_i32(kv_indptr)
+        kv_last_page_len = _host_i32(kv_last_page_len)
+        qo_indptr = _host_i32(qo_indptr)
+        q_start = _host_i32(q_start)
+        if kv_indices.dtype != torch.int32 or not kv_indices.is_cuda:
+            raise ValueError("kv_indices must be a device int32 tensor")
+        self._kv_indices = kv_indices.contiguous()
+        d = PlanDesc()
+        d.kind = PKV_DECODE if kind == "decode" else PKV_PREFILL
+        d.batch_size = len(kv_last_page_len)
+        d.qo_indptr = None if qo_indptr is None else qo_indptr.ctypes.data
+        d.kv_indptr = kv_indptr.ctypes.data
+        d.kv_last_page_len = kv_last_page_len.ctypes.data
+        d.q_start = None if q_start is None else q_start.ctypes.data
+        d.kv_indices = self._kv_indices.data_ptr() if self._kv_indices.numel() else None
+        d.num_pages = int(num_pages)
+        d.num_qo_heads = int(num_qo_heads)
+        d.num_kv_heads = int(num_kv_heads)
+        d.head_dim = int(head_dim)
+        d.page_size = int(page_size)
+        d.window_left = int(window_left)
+        d.causal = 1 if causal else 0
+        d.sm_scale = float(sm_scale if sm_scale is not None else head_dim ** -0.5)
+        d.fixed_split_size = int(fixed_split_size)
+        d.disable_split_kv = 1 if disable_split_kv else 0
+        d.dtype = PKV_BF16
+        _check(self._lib.pkv_plan_create(ctypes.byref(self._handle), ctypes.byref(d),
+                                         _stream_handle(stream)), "pkv_plan_create")
+        self.num_qo_heads = int(num_qo_heads)
+        self.head_dim = int(head_dim)
+        self.info = self.get_info()
+
+    def get_info(self) -> dict:
+        info = PlanInfo()
+        _check(self._lib.pkv_plan_get_info(self._handle, ctypes.byref(info)), "pkv_plan_get_info")
+        return {k: getattr(info, k) for k, _ in PlanInfo._fields_ if k != "reserved"}
+
+    def run(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+            return_lse: bool = False, stream=None):
+        """Attention for the planned batch; returns out (and lse when asked)."""
+        for t, name in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor")
+        if out is None:
+            out = torch.empty_like(q)
+        if return_lse and lse is None:
+            lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+        _check(self._lib.pkv_run(self._handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                 _ptr(lse), _stream_handle(stream)), "pkv_run")
+        return (out, lse) if (return_lse or lse is not None) else out
+
+    def set_timing_events(self, ev_begin, ev_end):
+        """Raw cudaEvent_t handles (ints) recorded around the main kernel of later runs."""
+        _check(self._lib.pkv_plan_set_timing_events(self._handle, ctypes.c_void_p(ev_begin or 0),
+                                                    ctypes.c_void_p(ev_end or 0)),
+               "pkv_plan_set_timing_events")
+
+    def device_status(self) -> int:
+        st = ctypes.c_int32(0)
+        _check(self._lib.pkv_plan_device_status(self._handle, ctypes.byref(st)),
+               "pkv_plan_device_status")
+        return st.value
+
+    def close(self):
+        if getattr(self, "_handle", None) is not None and self._handle.value:
+            self._lib.pkv_plan_destroy(self._handle)
+            self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def plan(**kw) -> Plan:
+    return Plan(**kw)
+
+
+def merge_state(v_a: torch.Tensor, s_a: torch.Tensor, v_b: torch.Tensor, s_b: torch.Tensor,
+                v_out: Optional[torch.Tensor] = None, s_out: Optional[torch.Tensor] = None,
+                stream=None):
+    """(v, s) = merge((v_a, s_a), (v_b, s_b)); v: [tokens, heads, d] bf16 or fp32."""
+    lib = load_library()
+    if v_a.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("values must be bf16 or fp32")
+    if v_a.shape != v_b.shape or v_a.dim() != 3 or s_a.shape != v_a.shape[:2] or s_b.shape != s_a.shape:
+        raise ValueError("shape mismatch")
+    if v_out is None:
+        v_out = torch.empty_like(v_a)
+    if s_out is None:
+        s_out = torch.empty_like(s_a)
+    dtype = PKV_BF16 if v_a.dtype == torch.bfloat16 else PKV_F32
+    _check(lib.pkv_merge_state(_ptr(v_a), _ptr(s_a), _ptr(v_b), _ptr(s_b), _ptr(v_out), _ptr(s_out),
+                               v_a.shape[0], v_a.shape[1], v_a.shape[2], dtype,
+                               _stream_handle(stream)), "pkv_merge_state")
+    return v_out, s_out
+
+
+def plan_for(w, device="cuda", **over) -> Plan:
+    """A Plan for a paged_kv_sliding_gb300.inputs.Workload (test/bench convenience)."""
+    kv_indices = torch.as_tensor(w.kv_indices, dtype=torch.int32).to(device)
+    args = dict(kind=w.kind, kv_indptr=w.kv_indptr, kv_indices=kv_indices,
+                kv_last_page_len=w.kv_last_page_len, num_qo_heads=w.num_qo_heads,
+                num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, page_size=w.page_size,
+                num_pages=w.num_pages, window_left=w.window_left, causal=w.causal,
+                sm_scale=w.sm_scale, qo_indptr=None if w.kind == "decode" else w.qo_indptr,
+                q_start=w.q_start)
+    args.update(over)
+    return Plan(**args)
