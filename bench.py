@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""Benchmark of paged sliding-window attention on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole hot path over the batch-decode workload: 64
+requests with kv_len ~ U[256, 4096], 32 query / 8 KV heads, head_dim 128, page 16,
+once for each window_left in {-1, 0, 31, 127, 1023} (plans made beforehand; each
+run = split-KV decode kernel + LSE merge kernel). The metric is the algorithmic KV
+bytes read (visible rows x 2 x H_kv x d x 2 B) per second. The line also carries
+the prefill (TFLOP/s) and long-context decode (GB/s) workloads under "workloads".
+
+L2 is flushed (a 512 MiB write) between timed steps, outside the timed events.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_sliding_gb300 import inputs as wl  # noqa: E402
+from paged_kv_sliding_gb300 import workcount  # noqa: E402
+
+METRIC = "prefill TFLOP/s + decode KV GB/s, paged SWA attn, 1 GB300, % of roofline"
+UNIT = "GB/s"
+WORKLOAD = ("batch decode: 64 requests, kv_len U[256,4096], 32q/8kv heads, d 128, page 16, "
+            "window_left in {-1,0,31,127,1023}, bf16, lse")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _profiled_traffic(kernel: str, workload: str, source: str):
+    """dram bytes per launch recorded by an ncu capture under profiles/, if the
+    recorded source hash still matches the kernel's source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    src = os.path.join(ROOT, "paged_kv_sliding_gb300", "csrc", source)
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return float(m.group(1)) if cur.startswith(h.group(1)) else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.idx = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _cudart():
+    import ctypes
+    for name in ("libcudart.so.13", "libcudart.so"):
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            continue
+    return None
+
+
+class RawEvent:
+    """A cudaEvent_t created through the CUDA runtime, for the library's timing hook."""
+    _rt = None
+
+    def __init__(self):
+        import ctypes
+        if RawEvent._rt is None:
+            RawEvent._rt = _cudart()
+        self.h = ctypes.c_void_p()
+        assert RawEvent._rt.cudaEventCreate(ctypes.byref(self.h)) == 0
+
+    def elapsed_ms(self, later: "RawEvent") -> float:
+        import ctypes
+        ms = ctypes.c_float()
+        assert RawEvent._rt.cudaEventElapsedTime(ctypes.byref(ms), self.h, later.h) == 0
+        return ms.value
+
+
+def _flush_l2(buf):
+    buf.zero_()
+
+
+# ------------------------------------------------------------------------------- ours
+
+def _timed_runs(runs, steps, warmup, flush):
+    """runs: list of (plan, args) executed back to back as one step. Returns
+    (per-step device ms list, main-kernel ms per run index summed over steps)."""
+    stream = torch.cuda.current_stream()
+    evs = [(RawEvent(), RawEvent()) for _ in runs]
+    for (plan, _), (b, e) in zip(runs, evs):
+        plan.set_timing_events(b.h.value, e.h.value)
+    for _ in range(warmup):
+        for plan, a in runs:
+            plan.run(*a)
+    torch.cuda.synchronize()
+    step_ms = []
+    kern_ms = [0.0] * len(runs)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(steps):
+        flush()
+        start.record(stream)
+        for plan, a in runs:
+            plan.run(*a)
+        end.record(stream)
+        end.synchronize()
+        step_ms.append(start.elapsed_time(end))
+        for i, (b, e) in enumerate(evs):
+            kern_ms[i] += b.elapsed_ms(e)
+    for plan, _ in runs:
+        plan.set_timing_events(None, None)
+    return step_ms, kern_ms
+
+
+def bench_decode_windows(pkv, w_base, windows, steps, warmup, flush):
+    plans, runs, bytes_per = [], [], []
+    out = torch.empty_like(w_base.q)
+    lse = torch.empty(w_base.q.shape[0], w_base.q.shape[1], dtype=torch.float32, device="cuda")
+    launches = 0
+    for W in windows:
+        w = w_base.with_window(W)
+        plan = pkv.plan_for(w)
+        plans.append(plan)
+        runs.append((plan, (w.q, w.k_cache, w.v_cache, out, lse)))
+        bytes_per.append(workcount.decode_kv_bytes(w))
+        launches += plan.info["kernels_per_run"]
+    step_ms, kern_ms = _timed_runs(runs, steps, warmup, flush)
+    return plans, runs, bytes_per, step_ms, kern_ms, launches
+
+
+def bench_prefill(pkv, w, steps, warmup, flush):
+    plan = pkv.plan_for(w)
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.q.shape[0], w.q.shape[1], dtype=torch.float32, device="cuda")
+    step_ms, kern_ms = _timed_runs([(plan, (w.q, w.k_cache, w.v_cache, out, lse))], steps, warmup, flush)
+    flops = workcount.attention_flops(w)
+    t = sum(kern_ms) / steps
+    return {"tflops": flops / (t * 1e-3) / 1e12, "kernel_ms": t, "algorithmic_gflop": flops / 1e9,
+            "work_items": plan.info["num_work_items"]}
+
+
+def e2e_decode(pkv, w_dev, windows, steps, warmup):
+    """Same step through the public API from pinned HOST buffers: H2D of q, the
+    paged K/V pool and the page ids, the five runs, D2H of out and lse."""
+    host = {k: getattr(w_dev, k).cpu().pin_memory() for k in ("q", "k_cache", "v_cache")}
+    idx_host = torch.as_tensor(w_dev.kv_indices, dtype=torch.int32).pin_memory()
+    dev = {k: torch.empty_like(getattr(w_dev, k)) for k in ("q", "k_cache", "v_cache")}
+    idx_dev = torch.empty_like(idx_host, device="cuda")
+    plans = [pkv.plan_for(w_dev.with_window(W), kv_indices=idx_dev) for W in windows]
+    outs = [torch.empty_like(w_dev.q) for _ in windows]
+    lses = [torch.empty(w_dev.q.shape[:2], dtype=torch.float32, device="cuda") for _ in windows]
+    out_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    lse_host = [torch.empty(l.shape, dtype=l.dtype).pin_memory() for l in lses]
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + idx_host.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in out_host + lse_host)
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        idx_dev.copy_(idx_host, non_blocking=True)
+        for p, o, l in zip(plans, outs, lses):
+            p.run(dev["q"], dev["k_cache"], dev["v_cache"], o, l)
+        for o, l, oh, lh in zip(outs, lses, out_host, lse_host):
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(l, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    return (time.perf_counter() - t0) / steps, h2d, d2h
+
+
+def run_ours(args, rank, world):
+    from paged_kv_sliding_gb300 import build, pkv
+    build.build()
+    pkv.load_library()
+    dev_index = torch.cuda.current_device()
+    peaks = _peaks()
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush = lambda: _flush_l2(flush_buf)  # noqa: E731
+
+    w = wl.batch_decode(-1, device="cuda")
+    windows = wl.BATCH_DECODE_WINDOWS
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        plans, runs, bytes_per, step_ms, kern_ms, launches = bench_decode_windows(
+            pkv, w, windows, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    step_bytes = sum(bytes_per)
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # dominant kernel: the decode kernel, averaged over its launches (all windows)
+    kern_total = sum(kern_ms) / args.steps
+    achieved = step_bytes / (kern_total * 1e-3) / 1e9
+    per_window = {str(W): {"kv_mb": b / 1e6, "kernel_us": 1e3 * k / args.steps,
+                           "gbs": b / (k / args.steps * 1e-3) / 1e9,
+                           "frac_hbm": b / (k / args.steps * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "splits": p.info["num_partials"], "ctas": p.info["num_work_items"]}
+                  for W, b, k, p in zip(windows, bytes_per, kern_ms, plans)}
+    traffic = _profiled_traffic("decode", "batch_decode", "pkv_decode.cu")
+
+    e2e_s, h2d, d2h = e2e_decode(pkv, w, windows, max(3, args.steps // 4), 2)
+    del plans, runs
+    torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "flushed between steps (512 MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "kernel": "pkv decode_kernel<128>",
+                     "peak_source": peaks["source"]},
+        "e2e": {"value": round(world * step_bytes / e2e_s / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * args.steps,
+        "per_window": per_window,
+    }
+    clocks = clk.summary()
+    if clocks:
+        line["clocks"] = clocks
+
+    if not args.no_extra:
+        line["workloads"] = extra_workloads(pkv, args, peaks, flush)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    return line
+
+
+def extra_workloads(pkv, args, peaks, flush):
+    res = {}
+    steps = max(3, min(args.steps, 10))
+    for P in (1, 16):
+        w = wl.swa_prefill(page_size=P, device="cuda")
+        r = bench_prefill(pkv, w, steps, 3, flush)
+        r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
+        res[f"swa_prefill_8x1500_d256_W511_p{P}"] = r
+        del w
+    w = wl.extend_with_prefix(device="cuda")
+    r = bench_prefill(pkv, w, steps, 3, flush)
+    r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
+    res["extend_prefix_16req_W4095"] = r
+    del w
+    torch.cuda.empty_cache()
+    for W in wl.LONG_DECODE_WINDOWS:
+        w = wl.long_decode(W, device="cuda")
+        plans, runs, bytes_per, step_ms, kern_ms, _ = bench_decode_windows(pkv, w, [W], steps, 2, flush)
+        k = kern_ms[0] / steps
+        res[f"long_decode_256x32768_W{W}"] = {
+            "gbs": bytes_per[0] / (k * 1e-3) / 1e9, "kernel_ms": k,
+            "step_ms": statistics.mean(step_ms), "kv_gb": bytes_per[0] / 1e9,
+            "frac_hbm": bytes_per[0] / (k * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "splits": plans[0].info["num_partials"], "ctas": plans[0].info["num_work_items"]}
+        del w, plans, runs
+        torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------------------- oracle
+
+def _oracle_decode_step(oracle, w, windows):
+    for W in windows:
+        oracle.attention(qo_indptr=w.qo_indptr, kv_indptr=w.kv_indptr, kv_indices=w.kv_indices,
+                         kv_last_page_len=w.kv_last_page_len, num_qo_heads=w.num_qo_heads,
+                         num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                         page_size=w.page_size, window_left=W, causal=w.causal,
+                         sm_scale=w.sm_scale, q=w.q, k_cache=w.k_cache, v_cache=w.v_cache)
+
+
+def cpu_baseline(args, budget_s: float = 12.0):
+    """The float64 oracle, as it stands, on this host's cores: the same batch-decode
+    step (all five windows, all 64 requests) repeated until about `budget_s`."""
+    import oracle
+    oracle.build()
+    cores = oracle.set_threads(0)
+    w = wl.batch_decode(-1)
+    windows = wl.BATCH_DECODE_WINDOWS
+    step_bytes = sum(workcount.decode_kv_bytes(w.with_window(W)) for W in windows)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_decode_step(oracle, w, windows)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or reps >= 20:
+            break
+    return {"value": round(reps * step_bytes / el / 1e9, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "sample": f"{reps} full batch-decode step(s) (64 requests x 5 windows), "
+                                        f"{el:.1f} s wall", "seconds": round(el, 2)}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    oracle.build()
+    cores = oracle.set_threads(0)
+    w = wl.batch_decode(-1)
+    windows = wl.BATCH_DECODE_WINDOWS
+    step_bytes = sum(workcount.decode_kv_bytes(w.with_window(W)) for W in windows)
+    for _ in range(args.warmup):
+        _oracle_decode_step(oracle, w, windows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_decode_step(oracle, w, windows)
+    el = time.perf_counter() - t0
+    value = step_bytes * args.steps / el / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} full batch-decode steps (64 requests x 5 windows)"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the prefill / long-decode workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # the oracle runs on host cores; for N > 1 only rank 0 runs it
+        line = run_reference(args, rank, world)
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
