@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
 
-SOURCES = ["pkv_api.cpp", "pkv_decode.cu", "pkv_merge.cu", "pkv_prefill.cu"]
+SOURCES = ["pkv_api.cpp", "pkv_decode.cu", "pkv_merge.cu", "pkv_prefill.cu", "pkv_prefill_pp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -33,9 +33,28 @@ def _nvcc():
 def _flags(extra_verbose=False):
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden", "--use_fast_math",
                 "-I", INCLUDE, "-I", CSRC, "-DNDEBUG"]
-    if extra_verbose:
-        f += ["-Xptxas", "-v"]
+    f += ["-Xptxas", "-v"]  # the register report is checked (see REGISTER_SPLIT)
     return f
+
+
+# Kernels that redistribute registers between warpgroups with setmaxnreg: the
+# launch allocation (threads x registers per thread) must be exactly what the
+# split assumes, or setmaxnreg.inc would wait for registers that never come.
+REGISTER_SPLIT = {"pkv_prefill_pp.cu": ("prefill_pp_kernel", 168)}
+
+
+def _check_register_split(logs):
+    import re
+    for src, (kernel, regs) in REGISTER_SPLIT.items():
+        log = logs[src]
+        blocks = re.findall(r"Compiling entry function '([^']+)'.*?Used (\d+) registers", log, re.S)
+        found = [(name, int(n)) for name, n in blocks if kernel in name]
+        if not found:
+            raise RuntimeError(f"no ptxas register report for {kernel}")
+        bad = [(name, n) for name, n in found if n != regs]
+        if bad:
+            raise RuntimeError(f"{kernel}: ptxas allocated {bad[0][1]} registers, the register "
+                               f"split assumes {regs}")
 
 
 def _deps_mtime():
@@ -61,6 +80,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))
+    _check_register_split(dict(zip(SOURCES, (log for _, log in results))))
     if verbose:
         for _, log in results:
             sys.stderr.write(log)

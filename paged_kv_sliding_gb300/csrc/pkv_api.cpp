@@ -103,6 +103,8 @@ int validate(const pkv_plan_desc *d, std::vector<HostRequest> &reqs)
         return fail(PKV_ERR_UNSUPPORTED, "dtype %d: only PKV_BF16 q/kv/out are supported", d->dtype);
     if (!(d->sm_scale == d->sm_scale) || std::isinf(d->sm_scale))
         return fail(PKV_ERR_INVALID_ARG, "sm_scale is not finite");
+    if (!(d->sm_scale > 0.f))
+        return fail(PKV_ERR_UNSUPPORTED, "sm_scale must be positive");
     if (d->kind == PKV_PREFILL &&
         d->num_qo_heads / d->num_kv_heads > kPrefillRows)
         return fail(PKV_ERR_UNSUPPORTED, "query-head group %d exceeds %d",
@@ -293,7 +295,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
 
     if (d.kind == PKV_PREFILL) {
         const int T = prefill_kv_tile(d.head_dim);
-        const int tq = std::max(1, kPrefillRows / group);
+        const int tq = prefill_tokens_per_cta(d.head_dim, group);
         for (int b = 0; b < B; ++b) {
             const HostRequest &r = reqs[b];
             for (int64_t t0 = 0; t0 < r.qo_len; t0 += tq) {
@@ -569,6 +571,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.num_kv_heads = d.num_kv_heads;
     p.group = d.num_qo_heads / d.num_kv_heads;
     p.tokens_per_tile = std::max(1, kPrefillRows / p.group);
+    p.total_q = (int32_t)plan->total_q;
     p.page_size = d.page_size;
     p.page_shift = page_shift_of(d.page_size);
     p.num_pages = d.num_pages;
@@ -576,7 +579,8 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
     if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
         return cuda_fail(ce, "cudaEventRecord");
-    ce = launch_prefill(p, d.head_dim, plan->mask_mode, plan->num_items, stream);
+    ce = d.head_dim <= 128 ? launch_prefill_pp(p, d.head_dim, plan->mask_mode, plan->num_items, stream)
+                           : launch_prefill(p, d.head_dim, plan->mask_mode, plan->num_items, stream);
     if (ce != cudaSuccess)
         return cuda_fail(ce, "prefill kernel launch");
     if (plan->ev_end && (ce = cudaEventRecord(plan->ev_end, stream)) != cudaSuccess)

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "pkv.h"
@@ -105,6 +107,7 @@ struct PrefillParams {
     int32_t page_shift;
     int32_t num_pages;
     int32_t window_left;
+    int32_t total_q;         // rows of q (bound of the query tensor map)
     float sm_scale_log2;
 };
 
@@ -117,7 +120,18 @@ cudaError_t launch_merge_state(const void *v_a, const float *s_a, const void *v_
 cudaError_t launch_prefill(const PrefillParams &p, int head_dim, int mask_mode, int num_items,
                            cudaStream_t s);
 
-// KV tile (tokens) of the prefill kernel for a head_dim.
+cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mode, int num_items,
+                              cudaStream_t s);
+// Page sizes whose pages the head_dim <= 128 prefill kernel loads with TMA boxes.
+bool prefill_pp_tma_page_size(int page_size);
+
+// KV tile (tokens) of the prefill kernels for a head_dim.
 int prefill_kv_tile(int head_dim);
+// Query tokens per prefill CTA: one 128-row tile (head_dim 256) or two (64, 128).
+inline int prefill_tokens_per_cta(int head_dim, int group)
+{
+    const int tq = group < kPrefillRows ? kPrefillRows / group : 1;
+    return head_dim <= 128 ? 2 * tq : tq;
+}
 
 }  // namespace pkv

@@ -1,4 +1,6 @@
-// Paged prefill / extend kernel on the 5th-generation tensor cores (tcgen05, TMEM).
+// Paged prefill / extend kernel on the 5th-generation tensor cores (tcgen05, TMEM),
+// one 128-row query tile per CTA; used for head_dim 256 (whose two O accumulators
+// would not fit TMEM next to S in the two-tile kernel).
 //
 // One CTA = 128 packed query rows (query tokens x the query heads that share one
 // KV head, the GQA packing of flashinfer_backend.py's should_use_tensor_core) of
@@ -431,12 +433,8 @@ int prefill_kv_tile(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 
 cudaError_t launch_prefill(const PrefillParams &p, int head_dim, int mask_mode, int num_items, cudaStream_t s)
 {
-    switch (head_dim) {
-    case 64: return launch_prefill_d<64>(p, mask_mode, num_items, s);
-    case 128: return launch_prefill_d<128>(p, mask_mode, num_items, s);
-    case 256: return launch_prefill_d<256>(p, mask_mode, num_items, s);
-    default: return cudaErrorInvalidValue;
-    }
+    // head_dim 64 and 128 run the two-tile kernel of pkv_prefill_pp.cu.
+    return head_dim == 256 ? launch_prefill_d<256>(p, mask_mode, num_items, s) : cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

@@ -64,6 +64,25 @@ def test_prefill_gqa(pkv, oracle_lib, group, P):
     check(pkv, oracle_lib, w)
 
 
+@pytest.mark.parametrize("P", [8, 32, 128, 256])
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_page_sizes(pkv, oracle_lib, P, d):
+    """Page sizes loaded as whole TMA boxes (8..128) or as parts of a page (256)."""
+    w = wl.make_workload(name="ps", qo_lens=[150, 37, 1], kv_lens=[700, 37, 300], num_qo_heads=8,
+                         num_kv_heads=2, head_dim=d, page_size=P, window_left=200, causal=True,
+                         seed=P + d)
+    check(pkv, oracle_lib, w)
+
+
+@pytest.mark.parametrize("heads", [(6, 2), (5, 1), (24, 8)])
+def test_prefill_odd_group(pkv, oracle_lib, heads):
+    """Query-head groups that do not divide the 128-row tile."""
+    w = wl.make_workload(name="odd", qo_lens=[100, 45], kv_lens=[230, 45], num_qo_heads=heads[0],
+                         num_kv_heads=heads[1], head_dim=128, page_size=16, window_left=60,
+                         causal=True, seed=sum(heads))
+    check(pkv, oracle_lib, w)
+
+
 @pytest.mark.parametrize("W", [-1, 3, 100])
 def test_prefill_non_causal(pkv, oracle_lib, W):
     w = wl.make_workload(name="nc", qo_lens=[40, 7], kv_lens=[300, 7], num_qo_heads=4,
