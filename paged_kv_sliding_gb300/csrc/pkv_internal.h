@@ -113,6 +113,8 @@ struct PrefillParams {
 
 // Launchers (one per kernel family); return cudaGetLastError() of the launch.
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s);
+// Page sizes whose pages the decode kernel loads with TMA boxes.
+bool decode_tma_page_size(int page_size);
 cudaError_t launch_merge_partials(const MergePartialsParams &p, int head_dim, cudaStream_t s);
 cudaError_t launch_merge_state(const void *v_a, const float *s_a, const void *v_b,
                                const float *s_b, void *v_out, float *s_out, int64_t rows,

@@ -162,24 +162,30 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillParams p)
                 need_mask |= j0 + T - 1 > p_min;
             if (kWindow)
                 need_mask |= j0 < p_max - p.window_left;
-            float m_tile = -INFINITY;
             if (need_mask) {
                 const int lo_c = kWindow ? pos - p.window_left - j0 : INT_MIN;
                 int hi_c = rq.kv_len - 1 - j0;
                 if (kCausal)
                     hi_c = min(hi_c, pos - j0);
 #pragma unroll
-                for (int c = 0; c < T; ++c) {
+                for (int c = 0; c < T; ++c)
                     s[c] = (c >= lo_c && c <= hi_c) ? s[c] * scale : -INFINITY;
-                    m_tile = fmaxf(m_tile, s[c]);
-                }
             } else {
 #pragma unroll
-                for (int c = 0; c < T; ++c) {
+                for (int c = 0; c < T; ++c)
                     s[c] *= scale;
-                    m_tile = fmaxf(m_tile, s[c]);
-                }
             }
+            float mx8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mx8[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+            for (int c = 16; c < T; c += 8)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mx8[k] = fmaxf(mx8[k], s[c + k]);
+            const float m_tile = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_cand = fmaxf(m_used, m_tile);
             const bool need = m_cand != -INFINITY && (m_used == -INFINITY || m_cand > m_used + 8.f);
             const float alpha = need ? fast_exp2(m_used - m_cand) : 1.f;
@@ -208,14 +214,14 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillParams p)
                 m_used = m_cand;
             }
             const float ref = m_used == -INFINITY ? 0.f : m_used;
-            float rowsum = 0.f;
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c8 = 0; c8 < T / 8; ++c8) {
                 float e[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     e[k] = fast_exp2(s[8 * c8 + k] - ref);
-                    rowsum += e[k];
+                    rs[k & 3] += e[k];
                 }
                 const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
                 const uint32_t w2 = pack_bf16(e[4], e[5]), w3 = pack_bf16(e[6], e[7]);
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillParams p)
                              "r"(w2), "r"(w3)
                              : "memory");
             }
-            l += rowsum;
+            l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B::kPFull));

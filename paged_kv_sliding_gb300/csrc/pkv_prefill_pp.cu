@@ -174,22 +174,28 @@ __global__ void __launch_bounds__(384, 1)
                     need_mask |= j0 + T - 1 > p_min;
                 if (kWindow)
                     need_mask |= j0 < p_max - p.window_left;
-                float m_raw = -INFINITY;
                 if (need_mask) {
                     const int lo_c = kWindow ? pos - p.window_left - j0 : INT_MIN;
                     int hi_c = rq.kv_len - 1 - j0;
                     if (kCausal)
                         hi_c = min(hi_c, pos - j0);
 #pragma unroll
-                    for (int c = 0; c < T; ++c) {
-                        s[c] = (c >= lo_c && c <= hi_c) ? s[c] : -INFINITY;
-                        m_raw = fmaxf(m_raw, s[c]);
-                    }
-                } else {
-#pragma unroll
                     for (int c = 0; c < T; ++c)
-                        m_raw = fmaxf(m_raw, s[c]);
+                        s[c] = (c >= lo_c && c <= hi_c) ? s[c] : -INFINITY;
                 }
+                // 8 independent max chains, then a tree: keeps the row max off a
+                // 128-long dependency chain.
+                float mx8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mx8[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+                for (int c = 16; c < T; c += 8)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mx8[k] = fmaxf(mx8[k], s[c + k]);
+                const float m_raw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                          fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float m_tile = m_raw == -INFINITY ? -INFINITY : m_raw * scale;
                 const float m_cand = fmaxf(m_used, m_tile);
                 const bool need = m_cand != -INFINITY && (m_used == -INFINITY || m_cand > m_used + 8.f);
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(384, 1)
                     m_used = m_cand;
                 }
                 const float nref = -(m_used == -INFINITY ? 0.f : m_used);
-                float rowsum = 0.f;
+                float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pw[32];
@@ -220,13 +226,13 @@ __global__ void __launch_bounds__(384, 1)
                     for (int k = 0; k < 32; ++k) {
                         const float e0 = fast_exp2(fmaf(s[64 * h + 2 * k], scale, nref));
                         const float e1 = fast_exp2(fmaf(s[64 * h + 2 * k + 1], scale, nref));
-                        rowsum += e0 + e1;
+                        rs[k & 3] += e0 + e1;
                         pw[k] = pack_bf16(e0, e1);
                     }
                     tmem_st32u(tS + 32 * h, pw);
                 }
                 tmem_wait_st();
-                l += rowsum;
+                l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
                 tc_fence_before();
                 mbar_arrive(bar(B::kPFull + wg));
             }
