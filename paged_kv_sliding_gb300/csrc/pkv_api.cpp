@@ -184,9 +184,14 @@ int device_sm_count(int device)
 }
 
 // Decode: pick the KV tokens per split. A pure function of the plan inputs and the
-// SM count: candidate split sizes are scored by a simulated makespan of the CTAs
-// (each costing its tokens plus a fixed overhead, plus the partial-state traffic
-// when split), and the smallest score wins.
+// SM count: every candidate split size (no split first, then from 256 tokens up
+// in steps of 1.25x) is scored by a simulated longest-first makespan of its CTAs
+// over the SM slots (each CTA costing its tokens plus a fixed start-up cost, plus
+// the partial-state traffic when split) plus a fixed cost for the merge pass
+// when any request splits; a candidate must beat the best so far by 2% to win,
+// which keeps splits rare unless they clearly pay (measured on GB300: a second
+// pass and many short CTAs cost more than the tail they remove on 64-request
+// batches).
 int64_t choose_decode_chunk(const std::vector<int64_t> &lens, int head_blocks, int sms,
                             int ctas_per_sm)
 {
@@ -196,15 +201,20 @@ int64_t choose_decode_chunk(const std::vector<int64_t> &lens, int head_blocks, i
     if (max_len <= 256)
         return std::max<int64_t>(max_len, 1);
     const int slots = sms * ctas_per_sm;
-    const double kCtaOverhead = 48.0;   // token-row equivalents per CTA
-    const double kPartialCost = 24.0;   // token-row equivalents per partial (write + merge read)
+    const double kCtaOverhead = 96.0;   // token-row equivalents per CTA
+    const double kPartialCost = 32.0;   // token-row equivalents per partial (write + merge read)
+    const double kMergeFixed = 512.0;   // the merge pass (launch and drain), per slot
+    std::vector<int64_t> cands{max_len};
+    for (int64_t c = 256; c < max_len; c = round_up((int64_t)(c * 1.25), 64))
+        cands.push_back(c);
     int64_t best_chunk = max_len;
-    double best = 1e300;
-    for (int64_t c = 256;; c = round_up((int64_t)(c * 1.25), 64)) {
-        int64_t chunk = std::min(c, max_len);
+    double best = 0;
+    bool have = false;
+    for (int64_t chunk : cands) {
         std::vector<double> costs;
         costs.reserve(lens.size() * 8);
         double merge = 0;
+        bool any_split = false;
         for (int64_t l : lens) {
             if (l <= 0) {
                 costs.push_back(kCtaOverhead);
@@ -219,16 +229,17 @@ int64_t choose_decode_chunk(const std::vector<int64_t> &lens, int head_blocks, i
                 for (int h = 0; h < head_blocks; ++h)
                     costs.push_back((double)t + kCtaOverhead + (n > 1 ? kPartialCost : 0.0));
             }
-            if (n > 1)
+            if (n > 1) {
                 merge += (double)n * head_blocks * kPartialCost / slots;
+                any_split = true;
+            }
         }
-        double score = simulate_makespan(costs, slots) + merge;
-        if (score < best * 0.995) {  // prefer fewer splits unless clearly better
+        double score = simulate_makespan(costs, slots) + merge + (any_split ? kMergeFixed : 0.0);
+        if (!have || score < best * 0.98) {
             best = score;
             best_chunk = chunk;
+            have = true;
         }
-        if (chunk >= max_len)
-            break;
     }
     return best_chunk;
 }

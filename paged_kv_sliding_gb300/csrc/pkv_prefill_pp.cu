@@ -20,8 +20,9 @@
 //     one thread execute in issue order, which makes S_i(j) complete only after
 //     O_i += P_i(j-1) V, the ordering every TMEM reuse below relies on.
 // Warps (384 threads): 0-3 softmax of Q0, 4-7 softmax of Q1 (thread = TMEM lane =
-// packed row), 8 TMEM allocation + MMA issue (+ zeroing of V rows past the cache
-// end in TMA mode), 9 TMA producer (9-11 gather with cp.async in the other mode).
+// packed row), 8 TMEM allocation + MMA issue (one lane), 9 TMA producer (also
+// zeroes V rows past the cache end in the last tile; 9-11 gather with cp.async in
+// the other mode).
 // Every wait is bounded (PKV_ERR_TIMEOUT, abort flag, MMA drain, TMEM freed).
 #include <cfloat>
 #include <climits>
@@ -65,7 +66,8 @@ struct PPBars {
     static constexpr int kSFull = kEmpty + NS;  // 2
     static constexpr int kPFull = kSFull + 2;   // 2
     static constexpr int kOFinal = kPFull + 2;
-    static constexpr int kDrain = kOFinal + 1;
+    static constexpr int kVZero = kOFinal + 1;  // last V tile's rows past the cache end zeroed
+    static constexpr int kDrain = kVZero + 1;
     static constexpr int kCount = kDrain + 1;
 };
 
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(bar(B::kPFull + i), 128);
         }
         mbar_init(bar(B::kOFinal), 1);
+        mbar_init(bar(B::kVZero), 1);
         mbar_init(bar(B::kDrain), 1);
         abort_flag = 0;
         no_abort = 0;
@@ -183,19 +186,22 @@ __global__ void __launch_bounds__(384, 1)
                     for (int c = 0; c < T; ++c)
                         s[c] = (c >= lo_c && c <= hi_c) ? s[c] : -INFINITY;
                 }
-                // 8 independent max chains, then a tree: keeps the row max off a
-                // 128-long dependency chain.
+                // 8 independent chains of three-input maxima, then a tree: the row
+                // max costs T/2 instructions and stays off a long dependency chain.
                 float mx8[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mx8[k] = fmaxf(s[k], s[k + 8]);
+                    mx8[k] = max3f(s[k], s[k + 8], s[k + 16]);
 #pragma unroll
-                for (int c = 16; c < T; c += 8)
+                for (int c = 24; c + 16 <= T; c += 16)
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mx8[k] = fmaxf(mx8[k], s[c + k]);
-                const float m_raw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                          fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                        mx8[k] = max3f(mx8[k], s[c + k], s[c + 8 + k]);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mx8[k] = fmaxf(mx8[k], s[T - 8 + k]);
+                const float m_raw = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                                          fmaxf(mx8[6], mx8[7]));
                 const float m_tile = m_raw == -INFINITY ? -INFINITY : m_raw * scale;
                 const float m_cand = fmaxf(m_used, m_tile);
                 const bool need = m_cand != -INFINITY && (m_used == -INFINITY || m_cand > m_used + 8.f);
@@ -218,21 +224,24 @@ __global__ void __launch_bounds__(384, 1)
                     m_used = m_cand;
                 }
                 const float nref = -(m_used == -INFINITY ? 0.f : m_used);
-                float rs[4] = {0.f, 0.f, 0.f, 0.f};
+                // Packed f32x2 arithmetic: one FMA and one add per two scores.
+                float rs[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pw[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const float e0 = fast_exp2(fmaf(s[64 * h + 2 * k], scale, nref));
-                        const float e1 = fast_exp2(fmaf(s[64 * h + 2 * k + 1], scale, nref));
-                        rs[k & 3] += e0 + e1;
+                        float x0, x1;
+                        fma2(x0, x1, s[64 * h + 2 * k], s[64 * h + 2 * k + 1], scale, scale, nref, nref);
+                        const float e0 = fast_exp2(x0);
+                        const float e1 = fast_exp2(x1);
+                        add2(rs[k & 3][0], rs[k & 3][1], e0, e1);
                         pw[k] = pack_bf16(e0, e1);
                     }
                     tmem_st32u(tS + 32 * h, pw);
                 }
                 tmem_wait_st();
-                l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+                l += ((rs[0][0] + rs[0][1]) + (rs[1][0] + rs[1][1])) + ((rs[2][0] + rs[2][1]) + (rs[3][0] + rs[3][1]));
                 tc_fence_before();
                 mbar_arrive(bar(B::kPFull + wg));
             }
@@ -278,103 +287,84 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 8) {
         // ------------------------------------------------------------ MMA issue
-        const uint32_t idesc_s = idesc_bf16_f32(128, T, false);
-        const uint32_t idesc_o = idesc_bf16_f32(128, D, true);
-        auto issue_s = [&](int i, uint32_t kslot) {
-            const uint32_t qb = sQ + i * Tr::kQTileBytes;
+        // One lane drives everything: waits, MMA issue and commits.
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(128, T, false);
+            const uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+            auto issue_s = [&](int i, uint32_t kslot) {
+                const uint32_t qb = sQ + i * Tr::kQTileBytes;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint64_t a = sdesc_sw128(qb + (k >> 2) * (128 * Tr::kChunk) + (k & 3) * 32, 16, 1024);
-                const uint64_t b = sdesc_sw128(kslot + (k >> 2) * (T * Tr::kChunk) + (k & 3) * 32, 16, 1024);
-                umma_f16(tmem + i * T, a, b, idesc_s, k > 0 ? 1u : 0u);
-            }
-            umma_commit(bar(B::kSFull + i));
-        };
-        auto issue_pv = [&](int i, uint32_t vslot, bool first) {
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t a = sdesc_sw128(qb + (k >> 2) * (128 * Tr::kChunk) + (k & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(kslot + (k >> 2) * (T * Tr::kChunk) + (k & 3) * 32, 16, 1024);
+                    umma_f16(tmem + i * T, a, b, idesc_s, k > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(B::kSFull + i));
+            };
+            auto issue_pv = [&](int i, uint32_t vslot, bool first) {
 #pragma unroll
-            for (int k = 0; k < T / 16; ++k) {
-                const uint64_t b = sdesc_sw128(vslot + k * (16 * Tr::kChunk), T * Tr::kChunk, 1024);
-                umma_f16_ts(tmem + Tr::kTmemO + i * D, tmem + i * T + k * 8, b, idesc_o,
-                            (!first || k > 0) ? 1u : 0u);
-            }
-        };
-        bool ok = true;
-        if (n_tiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kQ), 0, abort_v, kWaitLimitPP));
-            int sv_prev = 0;
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int nK = 2 * j, nV = 2 * j + 1;
-                const int sK = nK % NS, sV = nV % NS;
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kFull + sK), (nK / NS) & 1, abort_v, kWaitLimitPP));
-                if (!ok)
-                    break;
-                if (!TMA_KV)
-                    fence_proxy_async_smem();
-                tc_fence_after();
-                if (lane == 0)
-                    issue_s(0, slot(sK));
-                if (j > 0 && nq == 2) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kPFull + 1), (j - 1) & 1, abort_v, kWaitLimitPP));
-                    if (!ok)
+                for (int k = 0; k < T / 16; ++k) {
+                    const uint64_t b = sdesc_sw128(vslot + k * (16 * Tr::kChunk), T * Tr::kChunk, 1024);
+                    umma_f16_ts(tmem + Tr::kTmemO + i * D, tmem + i * T + k * 8, b, idesc_o,
+                                (!first || k > 0) ? 1u : 0u);
+                }
+            };
+            auto wait = [&](int b_idx, uint32_t parity) {
+                return mbar_wait(bar(b_idx), parity, abort_v, kWaitLimitPP);
+            };
+            bool ok = true;
+            if (n_tiles > 0) {
+                ok = wait(B::kQ, 0);
+                int sv_prev = 0;
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    const int nK = 2 * j, nV = 2 * j + 1;
+                    const int sK = nK % NS, sV = nV % NS;
+                    if (!(ok = wait(B::kFull + sK, (nK / NS) & 1)))
                         break;
+                    if (!TMA_KV)
+                        fence_proxy_async_smem();
                     tc_fence_after();
-                    if (lane == 0) {
+                    issue_s(0, slot(sK));
+                    if (j > 0 && nq == 2) {
+                        if (!(ok = wait(B::kPFull + 1, (j - 1) & 1)))
+                            break;
+                        tc_fence_after();
                         issue_pv(1, slot(sv_prev), j - 1 == 0);
                         umma_commit(bar(B::kEmpty + sv_prev));
                     }
-                }
-                if (lane == 0) {
                     if (nq == 2)
                         issue_s(1, slot(sK));
                     umma_commit(bar(B::kEmpty + sK));
-                }
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kFull + sV), (nV / NS) & 1, abort_v, kWaitLimitPP));
-                if (!ok)
-                    break;
-                const int j0 = (it.kv_tile_lo + j) * T;
-                if (TMA_KV && j0 + T > rq.kv_len) {
-                    // Rows past the end of the cache hold stale or foreign data; zero
-                    // them so that P = 0 never meets a non-finite value.
-                    const int vr = max(0, rq.kv_len - j0);
-                    const int n16 = (T - vr) * 8;  // 16-byte granules per chunk
-                    for (int idx = lane; idx < n16 * NCH; idx += 32) {
-                        const int c = idx / n16, e = idx % n16;
-                        const uint32_t a = slot(sV) + c * (T * Tr::kChunk) + (vr + e / 8) * Tr::kChunk + (e % 8) * 16;
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(a), "r"(0) : "memory");
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                if (!TMA_KV)
-                    fence_proxy_async_smem();
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kPFull + 0), j & 1, abort_v, kWaitLimitPP));
-                if (!ok)
-                    break;
-                tc_fence_after();
-                if (lane == 0) {
+                    if (!(ok = wait(B::kFull + sV, (nV / NS) & 1)))
+                        break;
+                    if (TMA_KV && j == n_tiles - 1 && (it.kv_tile_lo + j) * T + T > rq.kv_len &&
+                        !(ok = wait(B::kVZero, 0)))
+                        break;
+                    if (!TMA_KV)
+                        fence_proxy_async_smem();
+                    if (!(ok = wait(B::kPFull + 0, j & 1)))
+                        break;
+                    tc_fence_after();
                     issue_pv(0, slot(sV), j == 0);
                     if (nq == 1)
                         umma_commit(bar(B::kEmpty + sV));
+                    sv_prev = sV;
                 }
-                sv_prev = sV;
-            }
-            if (ok && nq == 2) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(bar(B::kPFull + 1), (n_tiles - 1) & 1, abort_v, kWaitLimitPP));
-                tc_fence_after();
-                if (ok && lane == 0) {
-                    issue_pv(1, slot(sv_prev), n_tiles - 1 == 0);
-                    umma_commit(bar(B::kEmpty + sv_prev));
+                if (ok && nq == 2) {
+                    ok = wait(B::kPFull + 1, (n_tiles - 1) & 1);
+                    tc_fence_after();
+                    if (ok) {
+                        issue_pv(1, slot(sv_prev), n_tiles - 1 == 0);
+                        umma_commit(bar(B::kEmpty + sv_prev));
+                    }
                 }
+                if (ok)
+                    umma_commit(bar(B::kOFinal));
             }
-            if (ok && lane == 0)
-                umma_commit(bar(B::kOFinal));
-        }
-        if (!ok && lane == 0) {
-            record_status(p.status, PKV_ERR_TIMEOUT);
-            abort_flag = 1;
-        }
-        if (lane == 0) {
+            if (!ok) {
+                record_status(p.status, PKV_ERR_TIMEOUT);
+                abort_flag = 1;
+            }
             umma_commit(bar(B::kDrain));
             mbar_wait(bar(B::kDrain), 0, &no_abort, kWaitLimitPP);
         }
@@ -442,6 +432,26 @@ __global__ void __launch_bounds__(384, 1)
                         }
                         if (isv == 0 && j + 1 < n_tiles)
                             pg_next = load_id(j + 1);
+                        if (isv == 1 && j == n_tiles - 1 && j0 + T > rq.kv_len) {
+                            // Rows past the end of the cache hold stale or foreign data;
+                            // once the tile has landed, zero them so that P = 0 never
+                            // meets a non-finite value, then release the MMA.
+                            okp = __all_sync(0xffffffffu, mbar_wait(bar(B::kFull + s), (n / NS) & 1, abort_v,
+                                                                    kWaitLimitPP));
+                            if (!okp)
+                                break;
+                            const int vr = max(0, rq.kv_len - j0);
+                            const int n16 = (T - vr) * 8;  // 16-byte granules per chunk
+                            for (int idx = lane; idx < n16 * NCH; idx += 32) {
+                                const int c = idx / n16, e = idx % n16;
+                                const uint32_t a = slot(s) + c * (T * Tr::kChunk) + (vr + e / 8) * Tr::kChunk + (e % 8) * 16;
+                                asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(a), "r"(0) : "memory");
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(bar(B::kVZero));
+                        }
                     }
                     if (!okp) {
                         if (lane == 0) {

@@ -67,6 +67,33 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
+// max(a, b, c) in one instruction (three-input max of sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float m;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+    return m;
+}
+
+// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1) as one packed f32x2 FMA.
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0,
+                                     float c1)
+{
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// (d0, d1) += (a0, a1) as one packed f32x2 add.
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1)
+{
+    asm("{\n .reg .b64 ra, rd;\n mov.b64 rd, {%0, %1};\n mov.b64 ra, {%2, %3};\n"
+        " add.rn.f32x2 rd, rd, ra;\n mov.b64 {%0, %1}, rd;\n}\n"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ void record_status(int32_t *status, int32_t code)
 {
     atomicCAS(status, 0, code);
