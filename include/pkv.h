@@ -188,6 +188,29 @@ PKV_API int pkv_plan_device_status(const pkv_plan *plan, int32_t *status);
  */
 PKV_API int pkv_plan_set_timing_events(pkv_plan *plan, void *ev_begin, void *ev_end);
 
+/*
+ * pkv_decode_noalloc: the decode of pkv_plan_create + pkv_run (desc->kind must be
+ * PKV_DECODE; same arguments, layouts and results) in one call that allocates no
+ * device memory: no cudaMalloc, cudaFree or allocating library routine. The pages
+ * have no counterpart to it. It is for callers that cannot allocate: serving
+ * processes whose memory pool already holds the device memory and forbids further
+ * driver allocations, and latency-critical paths that cannot pay for cudaMalloc /
+ * cudaFree, which may synchronise the whole device.
+ *
+ * The work list and the split-KV partial states live in a 32 MiB array of device
+ * memory that is part of the library image: every GPU on which the library is used
+ * holds it until the process exits. A batch that would need more than 32 MiB of it
+ * is rejected with PKV_ERR_UNSUPPORTED before any launch (pkv_last_error() gives
+ * the size; fewer splits, disable_split_kv, or pkv_plan_create + pkv_run handle it).
+ * The first call on a device looks up the array's device address (with that device
+ * current); make that first call before any stream capture. Every call shares the
+ * array: calls whose work overlaps on the GPU (other streams, or other host threads)
+ * race and must be serialised by the caller. Out-of-range page ids are skipped as
+ * in pkv_run, but this call has no device status to read them back.
+ */
+PKV_API int pkv_decode_noalloc(const pkv_plan_desc *desc, const void *q, const void *k_cache,
+                               const void *v_cache, void *out, float *lse, void *stream);
+
 /* Static name of a status code. */
 PKV_API const char *pkv_status_string(int status);
 

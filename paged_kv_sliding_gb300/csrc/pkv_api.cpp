@@ -47,6 +47,8 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 }  // namespace
 
+void pkv::set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
+
 struct pkv_plan {
     pkv_plan_desc desc{};  // host pointers cleared after planning
     int device = 0;

@@ -127,6 +127,9 @@ cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mod
 // Page sizes whose pages the head_dim <= 128 prefill kernel loads with TMA boxes.
 bool prefill_pp_tma_page_size(int page_size);
 
+// Set the calling thread's pkv_last_error() text.
+void set_last_error(const char *msg);
+
 // KV tile (tokens) of the prefill kernels for a head_dim.
 int prefill_kv_tile(int head_dim);
 // Query tokens per prefill CTA: one 128-row tile (head_dim 256) or two (64, 128).

@@ -33,7 +33,8 @@ PKV_F32 = 1
 
 EXPORTED = ("pkv_plan_create", "pkv_run", "pkv_merge_state", "pkv_plan_destroy",
             "pkv_plan_get_info", "pkv_plan_device_status", "pkv_status_string",
-            "pkv_last_error", "pkv_abi_version", "pkv_plan_set_timing_events")
+            "pkv_last_error", "pkv_abi_version", "pkv_plan_set_timing_events",
+            "pkv_decode_noalloc")
 
 
 class PkvError(RuntimeError):
@@ -113,6 +114,8 @@ def load_library(path: Optional[str] = None):
         lib.pkv_last_error.restype = ctypes.c_char_p
         lib.pkv_plan_set_timing_events.argtypes = [vp, vp, vp]
         lib.pkv_plan_set_timing_events.restype = ctypes.c_int
+        lib.pkv_decode_noalloc.argtypes = [ctypes.POINTER(PlanDesc), vp, vp, vp, vp, vp, vp]
+        lib.pkv_decode_noalloc.restype = ctypes.c_int
         lib.pkv_abi_version.argtypes = []
         lib.pkv_abi_version.restype = ctypes.c_int
         _lib = lib

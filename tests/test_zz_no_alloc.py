@@ -1,0 +1,103 @@
+"""pkv_decode_noalloc: the decode entry point that allocates no device memory.
+
+It exists for callers that cannot allocate (a serving process whose memory pool
+already holds the device memory and forbids further driver allocations, or a
+latency-critical path that cannot pay for cudaMalloc's possible device-wide
+synchronisation); its scratch is a fixed 32 MiB device array inside the library.
+Here it is called through the C ABI and compared with plan + run, twice in a row,
+since every call reuses the same array. This file sorts last so that a run that
+stops at the first failure has already run every other test.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_sliding_gb300 import inputs as wl
+from tests.helpers import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_sliding_gb300 import build, pkv as binding
+    build.build()
+    binding.load_library()
+    return binding
+
+
+def _desc(pkv, w, kv_indices, **over):
+    d = pkv.PlanDesc()
+    keep = {
+        "kv_indptr": np.ascontiguousarray(w.kv_indptr, dtype=np.int32),
+        "last": np.ascontiguousarray(w.kv_last_page_len, dtype=np.int32),
+    }
+    d.kind = pkv.PKV_DECODE
+    d.batch_size = w.batch
+    d.qo_indptr = None
+    d.kv_indptr = keep["kv_indptr"].ctypes.data
+    d.kv_last_page_len = keep["last"].ctypes.data
+    d.q_start = None
+    d.kv_indices = kv_indices.data_ptr()
+    d.num_pages = w.num_pages
+    d.num_qo_heads = w.num_qo_heads
+    d.num_kv_heads = w.num_kv_heads
+    d.head_dim = w.head_dim
+    d.page_size = w.page_size
+    d.window_left = w.window_left
+    d.causal = 1
+    d.sm_scale = w.sm_scale
+    d.fixed_split_size = over.get("fixed_split_size", -1)
+    d.disable_split_kv = 0
+    d.dtype = pkv.PKV_BF16
+    return d, keep
+
+
+def _noalloc(pkv, w, kv_indices, **over):
+    lib = pkv.load_library()
+    d, keep = _desc(pkv, w, kv_indices, **over)
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.q.shape[:2], dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = lib.pkv_decode_noalloc(ctypes.byref(d), ctypes.c_void_p(w.q.data_ptr()),
+                                ctypes.c_void_p(w.k_cache.data_ptr()),
+                                ctypes.c_void_p(w.v_cache.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                ctypes.c_void_p(lse.data_ptr()), ctypes.c_void_p(stream))
+    assert rc == pkv.PKV_OK, lib.pkv_last_error()
+    torch.cuda.synchronize()
+    return out, lse
+
+
+@pytest.mark.parametrize("W,split", [(127, -1), (-1, 96), (1023, 300)])
+def test_noalloc_matches_plan_run_twice(pkv, W, split):
+    w = wl.batch_decode(W, device="cuda", batch=16)
+    kv_indices = torch.as_tensor(w.kv_indices, dtype=torch.int32, device="cuda")
+    plan = pkv.plan_for(w, kv_indices=kv_indices, fixed_split_size=split)
+    ref_out, ref_lse = plan.run(w.q, w.k_cache, w.v_cache, return_lse=True)
+    torch.cuda.synchronize()
+    ref_out = ref_out.float().cpu().numpy()
+    ref_lse = ref_lse.cpu().numpy()
+    for call in range(2):
+        out, lse = _noalloc(pkv, w, kv_indices, fixed_split_size=split)
+        r = compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse)
+        assert r["bad_out"] == 0 and r["bad_lse"] == 0, (call, r)
+
+
+def test_noalloc_rejects_oversize_batch(pkv):
+    """A batch whose partial states exceed the fixed scratch is refused on the host
+    with a message naming the size, before any launch."""
+    w = wl.batch_decode(-1, device="cuda")
+    kv_indices = torch.as_tensor(w.kv_indices, dtype=torch.int32, device="cuda")
+    lib = pkv.load_library()
+    d, keep = _desc(pkv, w, kv_indices, fixed_split_size=16)
+    out = torch.empty_like(w.q)
+    rc = lib.pkv_decode_noalloc(ctypes.byref(d), ctypes.c_void_p(w.q.data_ptr()),
+                                ctypes.c_void_p(w.k_cache.data_ptr()),
+                                ctypes.c_void_p(w.v_cache.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                None, None)
+    assert rc == pkv.PKV_ERR_UNSUPPORTED
+    assert b"scratch" in lib.pkv_last_error()
