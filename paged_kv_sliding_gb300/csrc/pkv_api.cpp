@@ -66,6 +66,7 @@ struct pkv_plan {
     float *d_partial_o = nullptr;
     float *d_partial_lse = nullptr;
     int32_t *d_status = nullptr;
+    int32_t *d_counters = nullptr;  // split-KV arrival counters (fused merge)
     cudaEvent_t ev_begin = nullptr;  // optional timing events around the main kernel
     cudaEvent_t ev_end = nullptr;
 };
@@ -303,6 +304,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     std::vector<DecodeItem> d_items;
     std::vector<MergeItem> m_items;
     int num_partials = 0;
+    int num_counters = 0;
     int mask_mode = causal ? (W >= 0 ? kMaskCausalWindow : kMaskCausal)
                            : (W >= 0 ? kMaskWindow : kMaskNone);
 
@@ -357,11 +359,12 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
                                 : 0;
             if (L > 0)
                 n = (L + per - 1) / per;
-            int32_t pbase = -1;
+            int32_t pbase = -1, cbase = -1;
             if (n > 1) {
                 pbase = num_partials;
                 num_partials += (int32_t)n;
-                m_items.push_back({(int32_t)reqs[b].qo_begin, pbase, (int32_t)n, 0});
+                cbase = num_counters;  // one arrival counter per (KV head, head block)
+                num_counters += d.num_kv_heads * head_blocks;
             }
             for (int64_t s = 0; s < n; ++s) {
                 int64_t j0 = los[b] + s * per;
@@ -369,8 +372,9 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
                 for (int hk = 0; hk < d.num_kv_heads; ++hk)
                     for (int h0 = 0; h0 < group; h0 += kDecodeRows)
                         d_items.push_back({b, hk, hk * group + h0, std::min(kDecodeRows, group - h0),
-                                           (int32_t)j0, (int32_t)j1,
-                                           n > 1 ? (int32_t)(pbase + s) : -1, 0});
+                                           (int32_t)j0, (int32_t)j1, n > 1 ? (int32_t)(pbase + s) : -1,
+                                           pbase, (int32_t)n,
+                                           n > 1 ? cbase + hk * head_blocks + h0 / kDecodeRows : -1, 0, 0});
             }
         }
         std::stable_sort(d_items.begin(), d_items.end(), [](const DecodeItem &a, const DecodeItem &b) {
@@ -392,6 +396,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     const size_t o_merge = carve(sizeof(MergeItem) * std::max<size_t>(1, m_items.size()));
     const size_t o_po = carve(sizeof(float) * (size_t)num_partials * d.num_qo_heads * d.head_dim);
     const size_t o_pl = carve(sizeof(float) * (size_t)num_partials * d.num_qo_heads);
+    const size_t o_cnt = carve(sizeof(int32_t) * std::max(1, num_counters));
     const size_t o_status = carve(sizeof(int32_t) * 4);
     const size_t ws_bytes = off;
     const size_t upload_bytes = o_po;  // requests, items and merge items are uploaded
@@ -415,6 +420,8 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     ce = cudaMemcpyAsync(base, staging.data(), upload_bytes, cudaMemcpyHostToDevice, stream);
     if (ce == cudaSuccess)
         ce = cudaMemsetAsync(base + o_status, 0, sizeof(int32_t) * 4, stream);
+    if (ce == cudaSuccess)  // arrival counters start at zero; each merge resets its own
+        ce = cudaMemsetAsync(base + o_cnt, 0, sizeof(int32_t) * std::max(1, num_counters), stream);
     if (ce == cudaSuccess)
         ce = cudaStreamSynchronize(stream);  // the staging buffer is freed on return
     if (ce != cudaSuccess) {
@@ -440,6 +447,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     plan->d_partial_o = (float *)(base + o_po);
     plan->d_partial_lse = (float *)(base + o_pl);
     plan->d_status = (int32_t *)(base + o_status);
+    plan->d_counters = (int32_t *)(base + o_cnt);
     *out = plan;
     return PKV_OK;
 }
@@ -541,6 +549,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
         p.lse = lse;
         p.partial_o = plan->d_partial_o;
         p.partial_lse = plan->d_partial_lse;
+        p.merge_counters = plan->d_counters;
         p.status = plan->d_status;
         p.num_qo_heads = d.num_qo_heads;
         p.num_kv_heads = d.num_kv_heads;

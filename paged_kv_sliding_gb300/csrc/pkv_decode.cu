@@ -18,7 +18,10 @@
 //   compute warp w: tokens [16w, 16w + 16) of every tile, S = Q K^T and O += P V
 //     with mma.sync m16n8k16 (bf16 in, fp32 accumulate, rows = the query heads),
 //     running its own (m, l, O) without CTA-wide barriers; the four states are
-//     merged once at the end.
+//     merged once at the end. A CTA that handles one split of a request writes an
+//     fp32 partial state; the group's last CTA to finish (an arrival counter after
+//     a memory fence) combines the partials through their LSE, so no second
+//     kernel runs.
 // All waits are bounded; on expiry PKV_ERR_TIMEOUT is recorded and the CTA winds
 // down after its outstanding copies have landed.
 #include <cfloat>
@@ -406,6 +409,66 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
                     v.w = pack_bf16(acc[6], acc[7]);
                     *reinterpret_cast<uint4 *>(p.out + ((size_t)rq.qo_begin * p.num_qo_heads + h) * D + c) = v;
                 }
+            }
+        }
+        if (it.partial >= 0 && p.merge_counters) {
+            // Split-KV: the last CTA of this (request, KV head, head block) group to
+            // finish merges the group's partial states through their LSE (the
+            // merge_state of flashinfer_backend.py, n-way) and re-arms the counter.
+            __shared__ int last_flag;
+            asm volatile("bar.sync 1, 128;\n" ::: "memory");  // this CTA's partials are written
+            if (tid == 0) {
+                __threadfence();
+                last_flag = atomicAdd(p.merge_counters + it.counter, 1) == it.nsplit - 1;
+            }
+            asm volatile("bar.sync 1, 128;\n" ::: "memory");
+            if (last_flag) {
+                __threadfence();
+                constexpr int CPT = D / 8;  // columns per thread: 8 threads per head
+                const int r = tid >> 3, c0 = (tid & 7) * CPT;
+                if (r < it.nheads) {
+                    const int h = it.head0 + r;
+                    float mx = -INFINITY;
+                    for (int k = 0; k < it.nsplit; ++k)
+                        mx = fmaxf(mx, __ldcg(p.partial_lse + (size_t)(it.pbase + k) * p.num_qo_heads + h));
+                    float acc[CPT];
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e)
+                        acc[e] = 0.f;
+                    float sum = 0.f;
+                    if (mx != -INFINITY) {
+                        for (int k = 0; k < it.nsplit; ++k) {
+                            const size_t slot = (size_t)(it.pbase + k) * p.num_qo_heads + h;
+                            const float wgt = fast_exp2((__ldcg(p.partial_lse + slot) - mx) * 1.4426950408889634f);
+                            const float4 *src = reinterpret_cast<const float4 *>(p.partial_o + slot * D + c0);
+#pragma unroll
+                            for (int q4 = 0; q4 < CPT / 4; ++q4) {
+                                const float4 x = __ldcg(src + q4);
+                                acc[4 * q4 + 0] += wgt * x.x;
+                                acc[4 * q4 + 1] += wgt * x.y;
+                                acc[4 * q4 + 2] += wgt * x.z;
+                                acc[4 * q4 + 3] += wgt * x.w;
+                            }
+                            sum += wgt;
+                        }
+                    }
+                    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+                    uint16_t *dst = p.out + ((size_t)rq.qo_begin * p.num_qo_heads + h) * D + c0;
+#pragma unroll
+                    for (int q8 = 0; q8 < CPT / 8; ++q8) {
+                        uint4 v;
+                        v.x = pack_bf16(acc[8 * q8 + 0] * inv, acc[8 * q8 + 1] * inv);
+                        v.y = pack_bf16(acc[8 * q8 + 2] * inv, acc[8 * q8 + 3] * inv);
+                        v.z = pack_bf16(acc[8 * q8 + 4] * inv, acc[8 * q8 + 5] * inv);
+                        v.w = pack_bf16(acc[8 * q8 + 6] * inv, acc[8 * q8 + 7] * inv);
+                        reinterpret_cast<uint4 *>(dst)[q8] = v;
+                    }
+                    if (p.lse && (tid & 7) == 0)
+                        p.lse[(size_t)rq.qo_begin * p.num_qo_heads + h] =
+                            sum > 0.f ? mx + __log2f(sum) * 0.6931471805599453f : -INFINITY;
+                }
+                if (tid == 0)
+                    atomicExch(p.merge_counters + it.counter, 0);
             }
         }
     }

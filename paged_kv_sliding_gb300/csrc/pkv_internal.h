@@ -43,7 +43,10 @@ struct DecodeItem {
     int32_t nheads;   // query heads handled (<= kDecodeRows)
     int32_t j0, j1;   // key range, already clipped to the visible interval
     int32_t partial;  // -1: write out/lse directly; else partial slot of this split
-    int32_t pad;
+    int32_t pbase;    // first partial slot of the request (split items)
+    int32_t nsplit;   // splits of the request (split items)
+    int32_t counter;  // arrival counter of this (request, KV head, head block) group
+    int32_t pad0, pad1;
 };
 
 // Merge of a request's split-KV partial states into its output row.
@@ -70,6 +73,7 @@ struct DecodeParams {
     float *lse;          // may be null
     float *partial_o;    // [num_partials, num_qo_heads, head_dim]
     float *partial_lse;  // [num_partials, num_qo_heads]
+    int32_t *merge_counters;  // non-null: the last split CTA of a group merges its partials
     int32_t *status;
     int32_t num_qo_heads;
     int32_t num_kv_heads;

@@ -154,7 +154,8 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
             for (int hk = 0; hk < d->num_kv_heads; ++hk)
                 for (int h0 = 0; h0 < group; h0 += kDecodeRows)
                     items.push_back({b, hk, hk * group + h0, std::min(kDecodeRows, group - h0), (int32_t)j0,
-                                     (int32_t)j1, n > 1 ? (int32_t)(pbase + s) : -1, 0});
+                                     (int32_t)j1, n > 1 ? (int32_t)(pbase + s) : -1, pbase, (int32_t)n, -1, 0,
+                                     0});
         }
     }
     std::stable_sort(items.begin(), items.end(),
