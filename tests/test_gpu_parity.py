@@ -206,6 +206,18 @@ def test_batch_decode_full(pkv, oracle_lib, W):
     check(pkv, oracle_lib, wl.batch_decode(W))
 
 
+@pytest.mark.parametrize("P,d", [(16, 128), (4, 128), (16, 256), (1, 64)])
+def test_decode_many_short_items(pkv, oracle_lib, P, d):
+    """Short windows over many requests: several work items per CTA in one round."""
+    rng = np.random.default_rng(P * d)
+    kv = rng.integers(1, 300, size=300).tolist()
+    w = wl.make_workload(name="short", kind="decode", qo_lens=np.ones(len(kv)), kv_lens=kv,
+                         num_qo_heads=8, num_kv_heads=4, head_dim=d, page_size=P, window_left=40,
+                         causal=True, seed=P + d, layout_rng=rng)
+    _, info = check(pkv, oracle_lib, w)
+    assert info["num_work_items"] == 4 * len(kv)
+
+
 def test_decode_q_start_non_causal(pkv, oracle_lib):
     w = wl.make_workload(name="decq", kind="decode", qo_lens=np.ones(3), kv_lens=[100, 50, 10],
                          num_qo_heads=4, num_kv_heads=1, head_dim=64, page_size=8, window_left=7,
