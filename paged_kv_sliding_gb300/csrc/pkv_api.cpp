@@ -601,8 +601,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
     if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
         return cuda_fail(ce, "cudaEventRecord");
-    ce = d.head_dim <= 128 ? launch_prefill_pp(p, d.head_dim, plan->mask_mode, plan->num_items, stream)
-                           : launch_prefill(p, d.head_dim, plan->mask_mode, plan->num_items, stream);
+    ce = launch_prefill_pp(p, d.head_dim, plan->mask_mode, plan->num_items, stream);
     if (ce != cudaSuccess)
         return cuda_fail(ce, "prefill kernel launch");
     if (plan->ev_end && (ce = cudaEventRecord(plan->ev_end, stream)) != cudaSuccess)

@@ -123,13 +123,10 @@ cudaError_t launch_merge_partials(const MergePartialsParams &p, int head_dim, cu
 cudaError_t launch_merge_state(const void *v_a, const float *s_a, const void *v_b,
                                const float *s_b, void *v_out, float *s_out, int64_t rows,
                                int head_dim, int dtype, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillParams &p, int head_dim, int mask_mode, int num_items,
-                           cudaStream_t s);
-
 cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mode, int num_items,
                               cudaStream_t s);
-// Page sizes whose pages the head_dim <= 128 prefill kernel loads with TMA boxes.
-bool prefill_pp_tma_page_size(int page_size);
+// Page sizes whose pages the prefill kernel loads with TMA boxes.
+bool prefill_pp_tma_page_size(int page_size, int head_dim);
 
 // Set the calling thread's pkv_last_error() text.
 void set_last_error(const char *msg);

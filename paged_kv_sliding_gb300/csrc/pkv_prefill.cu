@@ -1,32 +1,31 @@
-// Paged prefill / extend kernel on the 5th-generation tensor cores (tcgen05, TMEM),
-// one 128-row query tile per CTA; used for head_dim 256 (whose two O accumulators
-// would not fit TMEM next to S in the two-tile kernel).
+// Paged prefill / extend kernel on the 5th-generation tensor cores: for head_dim
+// 64 and 128 two 128-row query tiles per CTA ping-pong over 128-key tiles; for
+// head_dim 256 (whose O accumulator takes half of TMEM) one query tile per CTA
+// runs over 64-key tiles.
 //
-// One CTA = 128 packed query rows (query tokens x the query heads that share one
-// KV head, the GQA packing of flashinfer_backend.py's should_use_tensor_core) of
-// one request, against the KV tiles the plan clipped to the rows' visible
-// interval [p_min - W, p_max] (whole tiles outside it are never loaded: the
-// tile-granular KV-start skip of sglang PR #31501, "What"). Tiles that straddle the
-// window edge, the causal diagonal or the end of the cache get the exact
-// per-element mask (the part the pages' bug compiled out); interior tiles skip it.
-//
-// Warp roles (256 threads):
-//   warps 0-3  softmax + epilogue: thread r owns packed row r = TMEM lane r.
-//              Reads S from TMEM, masks, keeps the fp32 running max m and sum l,
-//              writes P = exp2(s - m) as bf16 into shared memory (the A operand
-//              of the PV MMA), rescales O in TMEM only when m grows by more than
-//              2^8 (O and l always share the same reference max, so the result is
-//              exact), and finally writes out = O / l (bf16) and lse.
-//   warps 4-6  producers: cp.async 16-byte gathers of Q and of each K/V tile row
-//              through the page table (any page size), into 128-byte-swizzled
-//              tiles; completion is signalled on mbarriers.
-//   warp 7     TMEM allocation and the single MMA-issuing thread:
-//              S_j = Q K_j^T (M=128, N=T, K=16 per instruction) into a
-//              double-buffered TMEM S, then O += P_{j-1} V_{j-1} (M=128, N=D),
-//              so S of the next tile overlaps the softmax of the current one.
-// Every wait is bounded: on expiry the kernel records PKV_ERR_TIMEOUT, releases
-// the other roles through a shared abort flag, drains its MMAs, frees TMEM and
-// returns.
+// Same method as the single-tile kernel (plan-clipped KV tiles = the tile-granular
+// KV-start skip of sglang PR #31501, exact per-element mask on boundary tiles, fp32
+// online softmax with lazily rescaled O), laid out for throughput:
+//   * two query tiles Q0, Q1 (256 packed rows) share every K/V tile, halving K/V
+//     traffic per flop (head_dim 64 and 128);
+//   * P is written back into TMEM over the first half of its own S columns (bf16,
+//     two per column) and consumed by tcgen05.mma with the A operand in TMEM, so no
+//     shared memory is spent on P;
+//   * K and V tiles stream through a ring of 5 (head_dim 128, 256) or 8 (head_dim
+//     64) shared-memory slots, filled by TMA (a 4-D tensor map over the page pool,
+//     one box per page and 64-column chunk) when the page size is a multiple of 8
+//     that divides the KV tile (or is a multiple of it), else by cp.async
+//     gathers; Q always arrives by TMA (4-D map over [token, KV head, group, d]);
+//   * one thread issues, per KV tile j: S0(j) = Q0 K_j^T, O1 += P1(j-1) V_{j-1},
+//     S1(j) = Q1 K_j^T, O0 += P0(j) V_j, so the tensor core works on one query
+//     tile while the softmax warpgroup of the other runs. Tensor-core operations of
+//     one thread execute in issue order, which makes S_i(j) complete only after
+//     O_i += P_i(j-1) V, the ordering every TMEM reuse below relies on.
+// Warps (384 threads): 0-3 softmax of Q0, 4-7 softmax of Q1 (thread = TMEM lane =
+// packed row), 8 TMEM allocation + MMA issue (one lane), 9 TMA producer (also
+// zeroes V rows past the cache end in the last tile; 9-11 gather with cp.async in
+// the other mode).
+// Every wait is bounded (PKV_ERR_TIMEOUT, abort flag, MMA drain, TMEM freed).
 #include <cfloat>
 #include <climits>
 
@@ -37,50 +36,55 @@ namespace pkv {
 namespace {
 
 template <int D>
-struct PrefillTraits {
-    static constexpr int kM = kPrefillRows;            // packed query rows per CTA
-    static constexpr int kT = D >= 256 ? 64 : 128;     // KV tokens per tile
-    static constexpr int kStages = 2;
-    static constexpr int kChunk = 128;                 // bytes per swizzled row (64 bf16)
-    static constexpr int kQBytes = kM * D * 2;
-    static constexpr int kKVBytes = kT * D * 2;
-    static constexpr int kPBytes = kM * kT * 2;
+struct PPTraits {
+    static constexpr int kM = 128;            // packed rows per query tile
+    static constexpr int kT = D >= 256 ? 64 : 128;  // KV tokens per tile
+    static constexpr int kNQ = D >= 256 ? 1 : 2;    // query tiles per CTA (TMEM: S_i, O_i)
+    static constexpr int kChunk = 128;        // bytes per swizzled row
+    static constexpr int kNCh = D / 64;       // 64-column chunks
+    static constexpr int kQTileBytes = kM * D * 2;
+    static constexpr int kSlotBytes = kT * D * 2;
+    static constexpr int kSlots = D == 64 ? 8 : 5;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBytes;
-    static constexpr int kOffV = kOffK + kStages * kKVBytes;
-    static constexpr int kOffP = kOffV + kStages * kKVBytes;
-    static constexpr int kDynSmem = kOffP + kPBytes + 1024;  // + alignment slack
+    static constexpr int kOffSlots = kNQ * kQTileBytes;
+    static constexpr int kDynSmem = kOffSlots + kSlots * kSlotBytes + 1024;
+    static constexpr int kThreads = 384;
+    static constexpr int kProducers = 96;     // cp.async mode: warps 9-11
     static constexpr int kTmemCols = 512;
-    static constexpr int kTmemO = 256;                 // O columns; S buffer b at b * kT
-    static constexpr int kThreads = 256;
-    static constexpr int kProducers = 96;              // producer threads (warps 4-6)
-    static_assert(2 * kT <= kTmemO && kTmemO + D <= kTmemCols, "TMEM budget");
+    static constexpr int kTmemO = 256;        // O_i at kTmemO + i * D; S_i at i * kT
+    static_assert(kTmemO + kNQ * D <= kTmemCols && kNQ * kT <= kTmemO, "TMEM budget");
 };
 
-constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (about 2 s)
+constexpr long long kWaitLimitPP = 4000000000LL;
+constexpr int kRegsLaunch = 168;   // 65536 / 384 rounded down to a multiple of 8
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsOther = 96;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * kRegsLaunch, "register split");
 
-// Barrier slots.
-template <int S>
-struct Bars {
+template <int NS>
+struct PPBars {
     static constexpr int kQ = 0;
-    static constexpr int kKFull = 1;
-    static constexpr int kVFull = kKFull + S;
-    static constexpr int kKVEmpty = kVFull + S;
-    static constexpr int kSFull = kKVEmpty + S;  // 2
-    static constexpr int kPFull = kSFull + 2;
-    static constexpr int kPVDone = kPFull + 1;
-    static constexpr int kDrain = kPVDone + 1;
+    static constexpr int kFull = 1;
+    static constexpr int kEmpty = kFull + NS;
+    static constexpr int kSFull = kEmpty + NS;  // 2
+    static constexpr int kPFull = kSFull + 2;   // 2
+    static constexpr int kOFinal = kPFull + 2;
+    static constexpr int kVZero = kOFinal + 1;  // last V tile's rows past the cache end zeroed
+    static constexpr int kDrain = kVZero + 1;
     static constexpr int kCount = kDrain + 1;
 };
 
-template <int D, int MASK>
-__global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillParams p)
+template <int D, int MASK, bool TMA_KV>
+__global__ void __launch_bounds__(384, 1)
+    prefill_pp_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
 {
-    using Tr = PrefillTraits<D>;
-    using B = Bars<Tr::kStages>;
+    using Tr = PPTraits<D>;
+    constexpr int NS = Tr::kSlots;
+    using B = PPBars<NS>;
     constexpr int T = Tr::kT;
-    constexpr int S = Tr::kStages;
-    constexpr int CH = D / 8;  // 16-byte chunks per row
+    constexpr int NCH = Tr::kNCh;
+    constexpr int CH = D / 8;
     constexpr bool kCausal = MASK == kMaskCausal || MASK == kMaskCausalWindow;
     constexpr bool kWindow = MASK == kMaskCausalWindow || MASK == kMaskWindow;
 
@@ -92,10 +96,9 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillParams p)
 
     const uint32_t base = (smem_u32(dsmem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = base + Tr::kOffQ;
-    const uint32_t sK = base + Tr::kOffK;
-    const uint32_t sV = base + Tr::kOffV;
-    const uint32_t sP = base + Tr::kOffP;
+    const uint32_t sSlots = base + Tr::kOffSlots;
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    auto slot = [&](int s) { return sSlots + (uint32_t)s * Tr::kSlotBytes; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -103,27 +106,29 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillParams p)
     const RequestInfo rq = p.reqs[it.req];
     const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
     const int g = p.group;
-    const int valid_rows = it.ntok * g;
+    const int tq = p.tokens_per_tile;  // query tokens per 128-row tile
+    const int nq = (Tr::kNQ > 1 && it.ntok > tq) ? 2 : 1;
     const volatile int *abort_v = &abort_flag;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(B::kQ), Tr::kProducers);
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bar(B::kKFull + s), Tr::kProducers);
-            mbar_init(bar(B::kVFull + s), Tr::kProducers);
-            mbar_init(bar(B::kKVEmpty + s), 1);
+        mbar_init(bar(B::kQ), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(B::kFull + s), TMA_KV ? 1 : Tr::kProducers);
+            mbar_init(bar(B::kEmpty + s), 1);
         }
-        mbar_init(bar(B::kSFull + 0), 1);
-        mbar_init(bar(B::kSFull + 1), 1);
-        mbar_init(bar(B::kPFull), 128);
-        mbar_init(bar(B::kPVDone), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B::kSFull + i), 1);
+            mbar_init(bar(B::kPFull + i), 128);
+        }
+        mbar_init(bar(B::kOFinal), 1);
+        mbar_init(bar(B::kVZero), 1);
         mbar_init(bar(B::kDrain), 1);
         abort_flag = 0;
         no_abort = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
     }
-    if (warp == 7) {
+    if (warp == 8) {
         tmem_alloc(smem_u32(&tmem_base_s), Tr::kTmemCols);
         tmem_relinquish();
     }
@@ -132,315 +137,498 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillParams p)
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    if (warp < 4) {
+    // Register split: the block is launched with 384 x 168 registers (the build
+    // checks that ptxas allocated exactly 168); the softmax warpgroups take 200 and
+    // the MMA / producer warpgroup gives back down to 96: 256 x 200 + 128 x 96 =
+    // 63488 <= 64512.
+    if (warp >= 8)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsOther));
+    else
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsSoftmax));
+
+    if (warp < 8) {
         // ------------------------------------------------------------ softmax
-        const int r = threadIdx.x;
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-        const int tok = it.tok0 + r / g;
+        const int wg = warp >> 2;
+        const int r = threadIdx.x & 127;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + wg * T;
+        const uint32_t tO = tmem + lane_off + Tr::kTmemO + wg * D;
+        const int ntok_wg = min(tq, it.ntok - wg * tq);  // may be <= 0 for wg 1
+        const int tok = it.tok0 + wg * tq + r / g;
         const int pos = rq.q_start + tok;
-        const int p_min = rq.q_start + it.tok0;
-        const int p_max = p_min + it.ntok - 1;
+        const int p_min = rq.q_start + it.tok0 + wg * tq;
+        const int p_max = p_min + ntok_wg - 1;
         const float scale = p.sm_scale_log2;
         float m_used = -INFINITY;
         float l = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int buf = j & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull + buf), (j >> 1) & 1, abort_v, kWaitLimit));
-            if (!ok)
-                break;
-            tc_fence_after();
-            float s[T];
-#pragma unroll
-            for (int c = 0; c < T / 32; ++c)
-                tmem_ld32(t_lane + buf * T + 32 * c, *reinterpret_cast<float(*)[32]>(&s[32 * c]));
-            tmem_wait_ld();
-
-            const int j0 = (it.kv_tile_lo + j) * T;
-            bool need_mask = j0 + T > rq.kv_len;
-            if (kCausal)
-                need_mask |= j0 + T - 1 > p_min;
-            if (kWindow)
-                need_mask |= j0 < p_max - p.window_left;
-            if (need_mask) {
-                const int lo_c = kWindow ? pos - p.window_left - j0 : INT_MIN;
-                int hi_c = rq.kv_len - 1 - j0;
-                if (kCausal)
-                    hi_c = min(hi_c, pos - j0);
-#pragma unroll
-                for (int c = 0; c < T; ++c)
-                    s[c] = (c >= lo_c && c <= hi_c) ? s[c] * scale : -INFINITY;
-            } else {
-#pragma unroll
-                for (int c = 0; c < T; ++c)
-                    s[c] *= scale;
-            }
-            float mx8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mx8[k] = fmaxf(s[k], s[k + 8]);
-#pragma unroll
-            for (int c = 16; c < T; c += 8)
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mx8[k] = fmaxf(mx8[k], s[c + k]);
-            const float m_tile = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_cand = fmaxf(m_used, m_tile);
-            const bool need = m_cand != -INFINITY && (m_used == -INFINITY || m_cand > m_used + 8.f);
-            const float alpha = need ? fast_exp2(m_used - m_cand) : 1.f;
-
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kPVDone), (j - 1) & 1, abort_v, kWaitLimit));
+        if (wg < nq) {
+            for (int j = 0; j < n_tiles; ++j) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull + wg), j & 1, abort_v, kWaitLimitPP));
                 if (!ok)
                     break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
+                float s[T];
+#pragma unroll
+                for (int c = 0; c < T / 32; ++c)
+                    tmem_ld32(tS + 32 * c, *reinterpret_cast<float(*)[32]>(&s[32 * c]));
+                tmem_wait_ld();
+
+                const int j0 = (it.kv_tile_lo + j) * T;
+                bool need_mask = j0 + T > rq.kv_len;
+                if (kCausal)
+                    need_mask |= j0 + T - 1 > p_min;
+                if (kWindow)
+                    need_mask |= j0 < p_max - p.window_left;
+                if (need_mask) {
+                    const int lo_c = kWindow ? pos - p.window_left - j0 : INT_MIN;
+                    int hi_c = rq.kv_len - 1 - j0;
+                    if (kCausal)
+                        hi_c = min(hi_c, pos - j0);
+#pragma unroll
+                    for (int c = 0; c < T; ++c)
+                        s[c] = (c >= lo_c && c <= hi_c) ? s[c] : -INFINITY;
+                }
+                // 8 independent chains of three-input maxima, then a tree: the row
+                // max costs T/2 instructions and stays off a long dependency chain.
+                float mx8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mx8[k] = max3f(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+                for (int c = 24; c + 16 <= T; c += 16)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mx8[k] = max3f(mx8[k], s[c + k], s[c + 8 + k]);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mx8[k] = fmaxf(mx8[k], s[T - 8 + k]);
+                const float m_raw = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                                          fmaxf(mx8[6], mx8[7]));
+                const float m_tile = m_raw == -INFINITY ? -INFINITY : m_raw * scale;
+                const float m_cand = fmaxf(m_used, m_tile);
+                const bool need = m_cand != -INFINITY && (m_used == -INFINITY || m_cand > m_used + 8.f);
+                const float alpha = need ? fast_exp2(m_used - m_cand) : 1.f;
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    // O_i is stable: S_i(j) completed after O_i += P_i(j-1) V.
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
-                        tmem_ld32(t_lane + Tr::kTmemO + 32 * c, o);
+                        tmem_ld32(tO + 32 * c, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             o[e] *= alpha;
-                        tmem_st32(t_lane + Tr::kTmemO + 32 * c, o);
+                        tmem_st32(tO + 32 * c, o);
                     }
-                    tmem_wait_st();
                 }
-            }
-            if (need) {
-                l *= alpha;
-                m_used = m_cand;
-            }
-            const float ref = m_used == -INFINITY ? 0.f : m_used;
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c8 = 0; c8 < T / 8; ++c8) {
-                float e[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    e[k] = fast_exp2(s[8 * c8 + k] - ref);
-                    rs[k & 3] += e[k];
+                if (need) {
+                    l *= alpha;
+                    m_used = m_cand;
                 }
-                const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
-                const uint32_t w2 = pack_bf16(e[4], e[5]), w3 = pack_bf16(e[6], e[7]);
-                const uint32_t dst = sP + (c8 >> 3) * (Tr::kM * Tr::kChunk) + r * Tr::kChunk +
-                                     (((c8 & 7) ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst), "r"(w0), "r"(w1),
-                             "r"(w2), "r"(w3)
-                             : "memory");
+                const float nref = -(m_used == -INFINITY ? 0.f : m_used);
+                // Packed f32x2 arithmetic: one FMA and one add per two scores.
+                float rs[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+                for (int h = 0; h < T / 64; ++h) {
+                    uint32_t pw[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        float x0, x1;
+                        fma2(x0, x1, s[64 * h + 2 * k], s[64 * h + 2 * k + 1], scale, scale, nref, nref);
+                        const float e0 = fast_exp2(x0);
+                        const float e1 = fast_exp2(x1);
+                        add2(rs[k & 3][0], rs[k & 3][1], e0, e1);
+                        pw[k] = pack_bf16(e0, e1);
+                    }
+                    tmem_st32u(tS + 32 * h, pw);
+                }
+                tmem_wait_st();
+                l += ((rs[0][0] + rs[0][1]) + (rs[1][0] + rs[1][1])) + ((rs[2][0] + rs[2][1]) + (rs[3][0] + rs[3][1]));
+                tc_fence_before();
+                mbar_arrive(bar(B::kPFull + wg));
             }
-            l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(B::kPFull));
-        }
-        if (ok && n_tiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kPVDone), (n_tiles - 1) & 1, abort_v, kWaitLimit));
-            tc_fence_after();
-        }
-        if (!ok) {
-            record_status(p.status, PKV_ERR_TIMEOUT);
-            abort_flag = 1;
-        } else {
-            const bool row_ok = r < valid_rows;
-            const int h = it.kv_head * g + r % g;
-            const size_t orow = ((size_t)(rq.qo_begin + tok) * p.num_qo_heads + h);
-            uint16_t *dst = p.out + orow * D;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            if (ok && n_tiles > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kOFinal), 0, abort_v, kWaitLimitPP));
+                tc_fence_after();
+            }
+            if (!ok) {
+                record_status(p.status, PKV_ERR_TIMEOUT);
+                abort_flag = 1;
+            } else {
+                const bool row_ok = r < ntok_wg * g;
+                const int h = it.kv_head * g + r % g;
+                const size_t orow = (size_t)(rq.qo_begin + tok) * p.num_qo_heads + h;
+                uint16_t *dst = p.out + orow * D;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                if (n_tiles > 0) {
-                    tmem_ld32(t_lane + Tr::kTmemO + 32 * c, o);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        o[e] = 0.f;
-                }
-                if (row_ok) {
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 v;
-                        v.x = pack_bf16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
-                        v.y = pack_bf16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
-                        v.z = pack_bf16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
-                        v.w = pack_bf16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
-                        *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * q4) = v;
-                    }
-                }
-            }
-            if (row_ok && p.lse)
-                p.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-        }
-    } else if (warp < 7) {
-        // ------------------------------------------------------------ producers
-        constexpr int NP = Tr::kProducers;
-        const int pt = threadIdx.x - 128;
-        for (int idx = pt; idx < Tr::kM * CH; idx += NP) {
-            const int r = idx / CH, c = idx % CH;
-            const bool v = r < valid_rows;
-            const int rr = v ? r : 0;
-            const uint16_t *src = p.q + ((size_t)(rq.qo_begin + it.tok0 + rr / g) * p.num_qo_heads +
-                                         it.kv_head * g + rr % g) * D + c * 8;
-            const uint32_t dst = sQ + (c >> 3) * (Tr::kM * Tr::kChunk) + r * Tr::kChunk + (((c & 7) ^ (r & 7)) << 4);
-            cp_async_16(dst, src, v ? 16u : 0u);
-        }
-        cp_async_mbar_arrive(bar(B::kQ));
-
-        constexpr int kPerThread = (T * CH + NP - 1) / NP;  // 16-byte chunks per thread per tile
-        for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % S;
-            if (j >= S) {
-                if (!mbar_wait(bar(B::kKVEmpty + st), ((j / S) + 1) & 1, abort_v, kWaitLimit)) {
-                    record_status(p.status, PKV_ERR_TIMEOUT);
-                    abort_flag = 1;
-                    break;
-                }
-            }
-            const int j0 = (it.kv_tile_lo + j) * T;
-            size_t off[kPerThread];
-            uint32_t bytes[kPerThread];
-#pragma unroll
-            for (int k = 0; k < kPerThread; ++k) {
-                const int idx = pt + NP * k;
-                const int t = idx / CH, c = idx % CH;
-                const int jj = j0 + t;
-                off[k] = 0;
-                bytes[k] = 0;
-                if (idx < T * CH && jj < rq.kv_len) {
-                    const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
-                    const int slot = jj - lp * p.page_size;
-                    const int page = __ldg(p.kv_indices + rq.kv_page_begin + lp);
-                    if ((unsigned)page < (unsigned)p.num_pages) {
-                        off[k] = (((size_t)page * p.page_size + slot) * p.num_kv_heads + it.kv_head) * D + c * 8;
-                        bytes[k] = 16;
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    if (n_tiles > 0) {
+                        tmem_ld32(tO + 32 * c, o);
+                        tmem_wait_ld();
                     } else {
-                        record_status(p.status, PKV_ERR_DEVICE_BOUNDS);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = 0.f;
+                    }
+                    if (row_ok) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 v;
+                            v.x = pack_bf16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
+                            v.y = pack_bf16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+                            v.z = pack_bf16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+                            v.w = pack_bf16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
+                            *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * q4) = v;
+                        }
                     }
                 }
+                if (row_ok && p.lse)
+                    p.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
             }
-            const uint32_t kbase = sK + st * Tr::kKVBytes;
-            const uint32_t vbase = sV + st * Tr::kKVBytes;
-#pragma unroll
-            for (int k = 0; k < kPerThread; ++k) {
-                const int idx = pt + NP * k;
-                const int t = idx / CH, c = idx % CH;
-                const uint32_t so = (c >> 3) * (T * Tr::kChunk) + t * Tr::kChunk + (((c & 7) ^ (t & 7)) << 4);
-                if (idx < T * CH)
-                    cp_async_16(kbase + so, p.k_cache + off[k], bytes[k]);
-            }
-            cp_async_mbar_arrive(bar(B::kKFull + st));
-#pragma unroll
-            for (int k = 0; k < kPerThread; ++k) {
-                const int idx = pt + NP * k;
-                const int t = idx / CH, c = idx % CH;
-                const uint32_t so = (c >> 3) * (T * Tr::kChunk) + t * Tr::kChunk + (((c & 7) ^ (t & 7)) << 4);
-                if (idx < T * CH)
-                    cp_async_16(vbase + so, p.v_cache + off[k], bytes[k]);
-            }
-            cp_async_mbar_arrive(bar(B::kVFull + st));
         }
-        asm volatile("cp.async.wait_all;\n" ::: "memory");
-    } else {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ MMA issue
+        // One lane drives everything: waits, MMA issue and commits.
         if (lane == 0) {
-            const uint32_t idesc_s = idesc_bf16_f32(Tr::kM, T, false);
-            const uint32_t idesc_o = idesc_bf16_f32(Tr::kM, D, true);
-            bool ok = n_tiles == 0 || mbar_wait(bar(B::kQ), 0, abort_v, kWaitLimit);
-            for (int j = 0; ok && j <= n_tiles && n_tiles > 0; ++j) {
-                if (j < n_tiles) {
-                    const int st = j % S, buf = j & 1;
-                    ok = mbar_wait(bar(B::kKFull + st), (j / S) & 1, abort_v, kWaitLimit);
-                    if (!ok)
-                        break;
-                    fence_proxy_async_smem();
-                    tc_fence_after();
-                    const uint32_t kb = sK + st * Tr::kKVBytes;
+            const uint32_t idesc_s = idesc_bf16_f32(128, T, false);
+            const uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+            auto issue_s = [&](int i, uint32_t kslot) {
+                const uint32_t qb = sQ + i * Tr::kQTileBytes;
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint64_t a = sdesc_sw128(sQ + (k >> 2) * (Tr::kM * Tr::kChunk) + (k & 3) * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(kb + (k >> 2) * (T * Tr::kChunk) + (k & 3) * 32, 16, 1024);
-                        umma_f16(tmem + buf * T, a, b, idesc_s, k > 0 ? 1u : 0u);
-                    }
-                    umma_commit(bar(B::kSFull + buf));
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t a = sdesc_sw128(qb + (k >> 2) * (128 * Tr::kChunk) + (k & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(kslot + (k >> 2) * (T * Tr::kChunk) + (k & 3) * 32, 16, 1024);
+                    umma_f16(tmem + i * T, a, b, idesc_s, k > 0 ? 1u : 0u);
                 }
-                if (j >= 1) {
-                    const int i = j - 1, st = i % S;
-                    ok = mbar_wait(bar(B::kPFull), i & 1, abort_v, kWaitLimit) &&
-                         mbar_wait(bar(B::kVFull + st), (i / S) & 1, abort_v, kWaitLimit);
-                    if (!ok)
-                        break;
-                    fence_proxy_async_smem();
-                    tc_fence_after();
-                    const uint32_t vb = sV + st * Tr::kKVBytes;
+                umma_commit(bar(B::kSFull + i));
+            };
+            auto issue_pv = [&](int i, uint32_t vslot, bool first) {
 #pragma unroll
-                    for (int k = 0; k < T / 16; ++k) {
-                        const uint64_t a = sdesc_sw128(sP + (k >> 2) * (Tr::kM * Tr::kChunk) + (k & 3) * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(vb + k * (16 * Tr::kChunk), T * Tr::kChunk, 1024);
-                        umma_f16(tmem + Tr::kTmemO, a, b, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
-                    }
-                    umma_commit(bar(B::kPVDone));
-                    umma_commit(bar(B::kKVEmpty + st));
+                for (int k = 0; k < T / 16; ++k) {
+                    const uint64_t b = sdesc_sw128(vslot + k * (16 * Tr::kChunk), T * Tr::kChunk, 1024);
+                    umma_f16_ts(tmem + Tr::kTmemO + i * D, tmem + i * T + k * 8, b, idesc_o,
+                                (!first || k > 0) ? 1u : 0u);
                 }
+            };
+            auto wait = [&](int b_idx, uint32_t parity) {
+                return mbar_wait(bar(b_idx), parity, abort_v, kWaitLimitPP);
+            };
+            bool ok = true;
+            if (n_tiles > 0) {
+                ok = wait(B::kQ, 0);
+                int sv_prev = 0;
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    const int nK = 2 * j, nV = 2 * j + 1;
+                    const int sK = nK % NS, sV = nV % NS;
+                    if (!(ok = wait(B::kFull + sK, (nK / NS) & 1)))
+                        break;
+                    if (!TMA_KV)
+                        fence_proxy_async_smem();
+                    tc_fence_after();
+                    issue_s(0, slot(sK));
+                    if (j > 0 && nq == 2) {
+                        if (!(ok = wait(B::kPFull + 1, (j - 1) & 1)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(1, slot(sv_prev), j - 1 == 0);
+                        umma_commit(bar(B::kEmpty + sv_prev));
+                    }
+                    if (nq == 2)
+                        issue_s(1, slot(sK));
+                    umma_commit(bar(B::kEmpty + sK));
+                    if (!(ok = wait(B::kFull + sV, (nV / NS) & 1)))
+                        break;
+                    if (TMA_KV && j == n_tiles - 1 && (it.kv_tile_lo + j) * T + T > rq.kv_len &&
+                        !(ok = wait(B::kVZero, 0)))
+                        break;
+                    if (!TMA_KV)
+                        fence_proxy_async_smem();
+                    if (!(ok = wait(B::kPFull + 0, j & 1)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(0, slot(sV), j == 0);
+                    if (nq == 1)
+                        umma_commit(bar(B::kEmpty + sV));
+                    sv_prev = sV;
+                }
+                if (ok && nq == 2) {
+                    ok = wait(B::kPFull + 1, (n_tiles - 1) & 1);
+                    tc_fence_after();
+                    if (ok) {
+                        issue_pv(1, slot(sv_prev), n_tiles - 1 == 0);
+                        umma_commit(bar(B::kEmpty + sv_prev));
+                    }
+                }
+                if (ok)
+                    umma_commit(bar(B::kOFinal));
             }
             if (!ok) {
                 record_status(p.status, PKV_ERR_TIMEOUT);
                 abort_flag = 1;
             }
-            // Every MMA issued above has completed once this barrier flips.
             umma_commit(bar(B::kDrain));
-            mbar_wait(bar(B::kDrain), 0, &no_abort, kWaitLimit);
+            mbar_wait(bar(B::kDrain), 0, &no_abort, kWaitLimitPP);
         }
         __syncwarp();
+    } else {
+        // ------------------------------------------------------------ producers
+        const int pw = warp - 9;  // 0..2
+        if (pw == 0 && lane == 0 && n_tiles > 0) {
+            tma_prefetch_desc(&tm_q);
+            const uint32_t rows = (uint32_t)(g * tq);
+            mbar_arrive_expect_tx(bar(B::kQ), (uint32_t)nq * NCH * rows * Tr::kChunk);
+            for (int i = 0; i < nq; ++i)
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_4d(sQ + i * Tr::kQTileBytes + c * (128 * Tr::kChunk), &tm_q, c * 64, 0, it.kv_head,
+                                rq.qo_begin + it.tok0 + i * tq, bar(B::kQ));
+        }
+        if (TMA_KV) {
+            if (pw == 0 && n_tiles > 0) {
+                const int P = p.page_size;
+                const int rows_box = P < T ? P : T;
+                const int npg = T / rows_box;
+                const int n_pages_req = (rq.kv_len + P - 1) / P;
+                auto load_id = [&](int j) -> int {
+                    if (lane >= npg)
+                        return -1;
+                    const int j0 = (it.kv_tile_lo + j) * T;
+                    const int lp = P <= T ? j0 / P + lane : j0 / P;
+                    if (lp >= n_pages_req)
+                        return -1;
+                    const int pg = __ldg(p.kv_indices + rq.kv_page_begin + lp);
+                    if ((unsigned)pg >= (unsigned)p.num_pages) {
+                        record_status(p.status, PKV_ERR_DEVICE_BOUNDS);
+                        return -1;
+                    }
+                    return pg;
+                };
+                if (lane == 0) {
+                    tma_prefetch_desc(&tm_k);
+                    tma_prefetch_desc(&tm_v);
+                }
+                int pg = load_id(0);
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int j0 = (it.kv_tile_lo + j) * T;
+                    const int slot0 = P > T ? j0 % P : 0;
+                    int pg_next = -1;
+                    bool okp = true;
+                    for (int isv = 0; isv < 2; ++isv) {
+                        const int n = 2 * j + isv, s = n % NS;
+                        if (n >= NS) {
+                            okp = __all_sync(0xffffffffu, mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v,
+                                                                    kWaitLimitPP));
+                            if (!okp)
+                                break;
+                        }
+                        const unsigned valid = __ballot_sync(0xffffffffu, pg >= 0);
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(bar(B::kFull + s),
+                                                  (uint32_t)__popc(valid) * rows_box * Tr::kChunk * NCH);
+                        __syncwarp();
+                        if (pg >= 0) {
+                            const void *tm = isv ? (const void *)&tm_v : (const void *)&tm_k;
+                            for (int c = 0; c < NCH; ++c)
+                                tma_load_4d(slot(s) + c * (T * Tr::kChunk) + lane * rows_box * Tr::kChunk, tm,
+                                            c * 64, it.kv_head, slot0, pg, bar(B::kFull + s));
+                        }
+                        if (isv == 0 && j + 1 < n_tiles)
+                            pg_next = load_id(j + 1);
+                        if (isv == 1 && j == n_tiles - 1 && j0 + T > rq.kv_len) {
+                            // Rows past the end of the cache hold stale or foreign data;
+                            // once the tile has landed, zero them so that P = 0 never
+                            // meets a non-finite value, then release the MMA.
+                            okp = __all_sync(0xffffffffu, mbar_wait(bar(B::kFull + s), (n / NS) & 1, abort_v,
+                                                                    kWaitLimitPP));
+                            if (!okp)
+                                break;
+                            const int vr = max(0, rq.kv_len - j0);
+                            const int n16 = (T - vr) * 8;  // 16-byte granules per chunk
+                            for (int idx = lane; idx < n16 * NCH; idx += 32) {
+                                const int c = idx / n16, e = idx % n16;
+                                const uint32_t a = slot(s) + c * (T * Tr::kChunk) + (vr + e / 8) * Tr::kChunk + (e % 8) * 16;
+                                asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(a), "r"(0) : "memory");
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(bar(B::kVZero));
+                        }
+                    }
+                    if (!okp) {
+                        if (lane == 0) {
+                            record_status(p.status, PKV_ERR_TIMEOUT);
+                            abort_flag = 1;
+                        }
+                        break;
+                    }
+                    pg = pg_next;
+                }
+            }
+        } else if (n_tiles > 0) {
+            constexpr int NP = Tr::kProducers;
+            const int pt = threadIdx.x - 9 * 32;
+            // Work unit = one row and 8 consecutive 16-byte chunks (one 128-byte
+            // plane row): one page-table lookup feeds 8 copies.
+            constexpr int kUnits = T * (CH / 8);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int j0 = (it.kv_tile_lo + j) * T;
+                bool okp = true;
+                for (int isv = 0; isv < 2; ++isv) {
+                    const int n = 2 * j + isv, s = n % NS;
+                    if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP)) {
+                        okp = false;
+                        break;
+                    }
+                    const uint16_t *src = isv ? p.v_cache : p.k_cache;
+                    for (int u = pt; u < kUnits; u += NP) {
+                        const int t = u / (CH / 8), pl = u % (CH / 8);  // row, 64-column plane
+                        const int jj = j0 + t;
+                        size_t off = 0;
+                        uint32_t bytes = 0;
+                        if (jj < rq.kv_len) {
+                            const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
+                            const int sl = jj - lp * p.page_size;
+                            const int page = __ldg(p.kv_indices + rq.kv_page_begin + lp);
+                            if ((unsigned)page < (unsigned)p.num_pages) {
+                                off = (((size_t)page * p.page_size + sl) * p.num_kv_heads + it.kv_head) * D + pl * 64;
+                                bytes = 16;
+                            } else {
+                                record_status(p.status, PKV_ERR_DEVICE_BOUNDS);
+                            }
+                        }
+                        const uint32_t row_base = slot(s) + pl * (T * Tr::kChunk) + t * Tr::kChunk;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            cp_async_16(row_base + ((c ^ (t & 7)) << 4), src + off + c * 8, bytes);
+                    }
+                    cp_async_mbar_arrive(bar(B::kFull + s));
+                }
+                if (!okp) {
+                    record_status(p.status, PKV_ERR_TIMEOUT);
+                    abort_flag = 1;
+                    break;
+                }
+            }
+            asm volatile("cp.async.wait_all;\n" ::: "memory");
+        }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 7) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, Tr::kTmemCols);
     }
 }
 
-template <int D, int MASK>
-cudaError_t launch_prefill_dm(const PrefillParams &p, int num_items, cudaStream_t s)
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
-    using Tr = PrefillTraits<D>;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool encode_4d(CUtensorMap *m, const void *base, const cuuint64_t dims[4], const cuuint64_t strides[3],
+               const cuuint32_t box[4])
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int MASK, bool TMA_KV>
+cudaError_t launch_pp_dmt(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tv, int num_items, cudaStream_t s)
+{
+    using Tr = PPTraits<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MASK>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_pp_kernel<D, MASK, TMA_KV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kDynSmem);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    prefill_kernel<D, MASK><<<num_items, Tr::kThreads, Tr::kDynSmem, s>>>(p);
+    prefill_pp_kernel<D, MASK, TMA_KV><<<num_items, Tr::kThreads, Tr::kDynSmem, s>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t launch_prefill_d(const PrefillParams &p, int mask_mode, int num_items, cudaStream_t s)
+template <int D, bool TMA_KV>
+cudaError_t launch_pp_dt(const PrefillParams &p, int mask_mode, const CUtensorMap &tq, const CUtensorMap &tk,
+                         const CUtensorMap &tv, int num_items, cudaStream_t s)
 {
     switch (mask_mode) {
-    case kMaskNone: return launch_prefill_dm<D, kMaskNone>(p, num_items, s);
-    case kMaskCausal: return launch_prefill_dm<D, kMaskCausal>(p, num_items, s);
-    case kMaskCausalWindow: return launch_prefill_dm<D, kMaskCausalWindow>(p, num_items, s);
-    case kMaskWindow: return launch_prefill_dm<D, kMaskWindow>(p, num_items, s);
+    case kMaskNone: return launch_pp_dmt<D, kMaskNone, TMA_KV>(p, tq, tk, tv, num_items, s);
+    case kMaskCausal: return launch_pp_dmt<D, kMaskCausal, TMA_KV>(p, tq, tk, tv, num_items, s);
+    case kMaskCausalWindow: return launch_pp_dmt<D, kMaskCausalWindow, TMA_KV>(p, tq, tk, tv, num_items, s);
+    case kMaskWindow: return launch_pp_dmt<D, kMaskWindow, TMA_KV>(p, tq, tk, tv, num_items, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
+bool prefill_pp_tma_page_size(int page_size, int head_dim)
+{
+    const int T = prefill_kv_tile(head_dim);
+    if (page_size < 8 || page_size % 8 != 0)
+        return false;
+    return page_size <= T ? T % page_size == 0 : page_size % T == 0;
+}
+
 int prefill_kv_tile(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 
-cudaError_t launch_prefill(const PrefillParams &p, int head_dim, int mask_mode, int num_items, cudaStream_t s)
+cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mode, int num_items, cudaStream_t s)
 {
-    // head_dim 64 and 128 run the two-tile kernel of pkv_prefill_pp.cu.
-    return head_dim == 256 ? launch_prefill_d<256>(p, mask_mode, num_items, s) : cudaErrorInvalidValue;
+    const int g = p.group, tq = p.tokens_per_tile, Hkv = p.num_kv_heads, P = p.page_size;
+    const bool tma_kv = prefill_pp_tma_page_size(P, head_dim);
+    const int T = prefill_kv_tile(head_dim);
+    CUtensorMap tm_q{}, tm_k{}, tm_v{};
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)g, (cuuint64_t)Hkv,
+                                    (cuuint64_t)(p.total_q > 0 ? p.total_q : 1)};
+        const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)g * head_dim * 2,
+                                       (cuuint64_t)Hkv * g * head_dim * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)g, 1, (cuuint32_t)tq};
+        if (!encode_4d(&tm_q, p.q, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    if (tma_kv) {
+        const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)Hkv, (cuuint64_t)P,
+                                    (cuuint64_t)(p.num_pages > 0 ? p.num_pages : 1)};
+        const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)Hkv * head_dim * 2,
+                                       (cuuint64_t)P * Hkv * head_dim * 2};
+        const cuuint32_t box[4] = {64, 1, (cuuint32_t)(P < T ? P : T), 1};
+        if (!encode_4d(&tm_k, p.k_cache, dims, strides, box) || !encode_4d(&tm_v, p.v_cache, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    switch (head_dim) {
+    case 64:
+        return tma_kv ? launch_pp_dt<64, true>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s)
+                      : launch_pp_dt<64, false>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s);
+    case 128:
+        return tma_kv ? launch_pp_dt<128, true>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s)
+                      : launch_pp_dt<128, false>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s);
+    case 256:
+        return tma_kv ? launch_pp_dt<256, true>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s)
+                      : launch_pp_dt<256, false>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace pkv
