@@ -56,6 +56,7 @@ struct pkv_plan {
     int num_items = 0;
     int num_partials = 0;
     int num_merge_items = 0;
+    int num_ctas = 0;  // prefill: persistent CTAs
     int64_t total_q = 0;
     const int32_t *kv_indices = nullptr;  // borrowed device pointer
     void *workspace = nullptr;
@@ -63,6 +64,7 @@ struct pkv_plan {
     RequestInfo *d_reqs = nullptr;
     void *d_items = nullptr;
     MergeItem *d_merge = nullptr;
+    int32_t *d_cta_items = nullptr;
     float *d_partial_o = nullptr;
     float *d_partial_lse = nullptr;
     int32_t *d_status = nullptr;
@@ -303,6 +305,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     std::vector<PrefillItem> p_items;
     std::vector<DecodeItem> d_items;
     std::vector<MergeItem> m_items;
+    std::vector<int32_t> cta_items;  // prefill: per-CTA item offsets
     int num_partials = 0;
     int num_counters = 0;
     int mask_mode = causal ? (W >= 0 ? kMaskCausalWindow : kMaskCausal)
@@ -326,10 +329,38 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
                     p_items.push_back({b, hk, (int32_t)t0, (int32_t)nt, tlo, thi, 0, 0});
             }
         }
-        // Longest first, so the last wave is made of short items.
-        std::stable_sort(p_items.begin(), p_items.end(), [](const PrefillItem &a, const PrefillItem &b) {
-            return (a.kv_tile_hi - a.kv_tile_lo) > (b.kv_tile_hi - b.kv_tile_lo);
-        });
+        // Persistent CTAs, one per SM: longest-processing-time-first assignment of
+        // the items to the least loaded CTA. Cost of an item in KV-tile steps: a
+        // single query tile runs its softmax-bound chain alone (about 0.65 of the
+        // two-tile ping-pong step), plus a fixed cost per item (pipeline fill and
+        // epilogue).
+        const int tq_tile = std::max(1, kPrefillRows / group);
+        auto cost = [&](const PrefillItem &it) {
+            const int nq = (d.head_dim <= 128 && it.ntok > tq_tile) ? 2 : 1;
+            return (it.kv_tile_hi - it.kv_tile_lo) * (nq == 2 ? 1.0 : 0.65) + 1.5;
+        };
+        std::stable_sort(p_items.begin(), p_items.end(),
+                         [&](const PrefillItem &a, const PrefillItem &b) { return cost(a) > cost(b); });
+        const int n_sm = device_sm_count(device);
+        const int G = (int)std::min<size_t>(p_items.size(), (size_t)n_sm);
+        std::vector<std::vector<PrefillItem>> per_cta(G);
+        std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>,
+                            std::greater<std::pair<double, int>>>
+            heap;
+        for (int c = 0; c < G; ++c)
+            heap.push({0.0, c});
+        for (const PrefillItem &it : p_items) {
+            auto [load, c] = heap.top();
+            heap.pop();
+            per_cta[c].push_back(it);
+            heap.push({load + cost(it), c});
+        }
+        p_items.clear();
+        cta_items.assign(1, 0);
+        for (int c = 0; c < G; ++c) {
+            p_items.insert(p_items.end(), per_cta[c].begin(), per_cta[c].end());
+            cta_items.push_back((int32_t)p_items.size());
+        }
     } else {
         const int head_blocks = (group + kDecodeRows - 1) / kDecodeRows;
         std::vector<int64_t> lens(B), los(B);
@@ -394,6 +425,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     const size_t o_reqs = carve(sizeof(RequestInfo) * std::max<size_t>(1, B));
     const size_t o_items = carve(item_bytes * std::max<size_t>(1, n_items));
     const size_t o_merge = carve(sizeof(MergeItem) * std::max<size_t>(1, m_items.size()));
+    const size_t o_cta = carve(sizeof(int32_t) * std::max<size_t>(1, cta_items.size()));
     const size_t o_po = carve(sizeof(float) * (size_t)num_partials * d.num_qo_heads * d.head_dim);
     const size_t o_pl = carve(sizeof(float) * (size_t)num_partials * d.num_qo_heads);
     const size_t o_cnt = carve(sizeof(int32_t) * std::max(1, num_counters));
@@ -416,6 +448,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     else
         std::memcpy(staging.data() + o_items, d_items.data(), item_bytes * n_items);
     std::memcpy(staging.data() + o_merge, m_items.data(), sizeof(MergeItem) * m_items.size());
+    std::memcpy(staging.data() + o_cta, cta_items.data(), sizeof(int32_t) * cta_items.size());
     uint8_t *base = (uint8_t *)plan->workspace;
     ce = cudaMemcpyAsync(base, staging.data(), upload_bytes, cudaMemcpyHostToDevice, stream);
     if (ce == cudaSuccess)
@@ -438,12 +471,14 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     plan->num_items = (int)n_items;
     plan->num_partials = num_partials;
     plan->num_merge_items = (int)m_items.size();
+    plan->num_ctas = cta_items.empty() ? 0 : (int)cta_items.size() - 1;
     plan->total_q = total_q;
     plan->kv_indices = d.kv_indices;
     plan->workspace_bytes = ws_bytes;
     plan->d_reqs = (RequestInfo *)(base + o_reqs);
     plan->d_items = base + o_items;
     plan->d_merge = (MergeItem *)(base + o_merge);
+    plan->d_cta_items = (int32_t *)(base + o_cta);
     plan->d_partial_o = (float *)(base + o_po);
     plan->d_partial_lse = (float *)(base + o_pl);
     plan->d_status = (int32_t *)(base + o_status);
@@ -581,6 +616,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     }
     PrefillParams p{};
     p.items = (const PrefillItem *)plan->d_items;
+    p.cta_items = plan->d_cta_items;
     p.reqs = plan->d_reqs;
     p.kv_indices = plan->kv_indices;
     p.q = (const uint16_t *)q;
@@ -601,7 +637,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
     if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
         return cuda_fail(ce, "cudaEventRecord");
-    ce = launch_prefill_pp(p, d.head_dim, plan->mask_mode, plan->num_items, stream);
+    ce = launch_prefill_pp(p, d.head_dim, plan->mask_mode, plan->num_ctas, stream);
     if (ce != cudaSuccess)
         return cuda_fail(ce, "prefill kernel launch");
     if (plan->ev_end && (ce = cudaEventRecord(plan->ev_end, stream)) != cudaSuccess)

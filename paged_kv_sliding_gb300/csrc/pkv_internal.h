@@ -94,7 +94,8 @@ struct MergePartialsParams {
 };
 
 struct PrefillParams {
-    const PrefillItem *items;
+    const PrefillItem *items;    // grouped by CTA
+    const int32_t *cta_items;    // CTA c runs items [cta_items[c], cta_items[c + 1])
     const RequestInfo *reqs;
     const int32_t *kv_indices;
     const uint16_t *q;
@@ -123,7 +124,8 @@ cudaError_t launch_merge_partials(const MergePartialsParams &p, int head_dim, cu
 cudaError_t launch_merge_state(const void *v_a, const float *s_a, const void *v_b,
                                const float *s_b, void *v_out, float *s_out, int64_t rows,
                                int head_dim, int dtype, cudaStream_t s);
-cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mode, int num_items,
+// One persistent CTA per entry of cta_items (num_ctas + 1 offsets).
+cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mode, int num_ctas,
                               cudaStream_t s);
 // Page sizes whose pages the prefill kernel loads with TMA boxes.
 bool prefill_pp_tma_page_size(int page_size, int head_dim);

@@ -1,11 +1,15 @@
 // Paged prefill / extend kernel on the 5th-generation tensor cores: for head_dim
-// 64 and 128 two 128-row query tiles per CTA ping-pong over 128-key tiles; for
-// head_dim 256 (whose O accumulator takes half of TMEM) one query tile per CTA
-// runs over 64-key tiles.
+// 64 and 128 two 128-row query tiles per work item ping-pong over 128-key tiles;
+// for head_dim 256 (whose O accumulator takes half of TMEM) one query tile per
+// work item runs over 64-key tiles.
 //
-// Same method as the single-tile kernel (plan-clipped KV tiles = the tile-granular
-// KV-start skip of sglang PR #31501, exact per-element mask on boundary tiles, fp32
-// online softmax with lazily rescaled O), laid out for throughput:
+// Method: plan-clipped KV tiles (the tile-granular KV-start skip of sglang PR
+// #31501), the exact per-element mask on boundary tiles, fp32 online softmax with
+// lazily rescaled O. Laid out for throughput:
+//   * persistent: one CTA per SM walks its own list of work items (balanced by the
+//     plan), so TMEM allocation, barrier set-up and the K/V ring are paid once per
+//     CTA, the next item's Q and first K/V tiles land while the current item
+//     finishes, and an item's epilogue overlaps the next item's first S = Q K^T;
 //   * two query tiles Q0, Q1 (256 packed rows) share every K/V tile, halving K/V
 //     traffic per flop (head_dim 64 and 128);
 //   * P is written back into TMEM over the first half of its own S columns (bf16,
@@ -21,10 +25,9 @@
 //     tile while the softmax warpgroup of the other runs. Tensor-core operations of
 //     one thread execute in issue order, which makes S_i(j) complete only after
 //     O_i += P_i(j-1) V, the ordering every TMEM reuse below relies on.
-// Warps (384 threads): 0-3 softmax of Q0, 4-7 softmax of Q1 (thread = TMEM lane =
-// packed row), 8 TMEM allocation + MMA issue (one lane), 9 TMA producer (also
-// zeroes V rows past the cache end in the last tile; 9-11 gather with cp.async in
-// the other mode).
+// Warps (384 threads): 0-3 softmax + epilogue of Q0, 4-7 of Q1 (thread = TMEM
+// lane = packed row), 8 TMEM allocation, Q loads and MMA issue (one lane), 9 TMA
+// producer of K/V (9-11 gather with cp.async in the other mode).
 // Every wait is bounded (PKV_ERR_TIMEOUT, abort flag, MMA drain, TMEM freed).
 #include <cfloat>
 #include <climits>
@@ -66,11 +69,12 @@ struct PPBars {
     static constexpr int kQ = 0;
     static constexpr int kFull = 1;
     static constexpr int kEmpty = kFull + NS;
-    static constexpr int kSFull = kEmpty + NS;  // 2
-    static constexpr int kPFull = kSFull + 2;   // 2
-    static constexpr int kOFinal = kPFull + 2;
-    static constexpr int kVZero = kOFinal + 1;  // last V tile's rows past the cache end zeroed
-    static constexpr int kDrain = kVZero + 1;
+    static constexpr int kSFull = kEmpty + NS;   // 2: S_i(j) complete in TMEM
+    static constexpr int kPFull = kSFull + 2;    // 2: P_i(j) written to TMEM (128 arrivals)
+    static constexpr int kOFinal = kPFull + 2;   // 2: O_i of the item complete
+    static constexpr int kOEmpty = kOFinal + 2;  // 2: O_i read out by the epilogue (128 arrivals)
+    static constexpr int kVLand = kOEmpty + 2;   // producer only: a tail V tile has landed
+    static constexpr int kDrain = kVLand + 1;
     static constexpr int kCount = kDrain + 1;
 };
 
@@ -102,12 +106,12 @@ __global__ void __launch_bounds__(384, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const PrefillItem it = p.items[blockIdx.x];
-    const RequestInfo rq = p.reqs[it.req];
-    const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
+    // This CTA's work items, in order (the plan balances the lists over the CTAs).
+    const int item_lo = p.cta_items[blockIdx.x];
+    const int item_hi = p.cta_items[blockIdx.x + 1];
     const int g = p.group;
     const int tq = p.tokens_per_tile;  // query tokens per 128-row tile
-    const int nq = (Tr::kNQ > 1 && it.ntok > tq) ? 2 : 1;
+    auto q_tiles = [&](const PrefillItem &it) { return (Tr::kNQ > 1 && it.ntok > tq) ? 2 : 1; };
     const volatile int *abort_v = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -119,9 +123,10 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B::kSFull + i), 1);
             mbar_init(bar(B::kPFull + i), 128);
+            mbar_init(bar(B::kOFinal + i), 1);
+            mbar_init(bar(B::kOEmpty + i), 128);
         }
-        mbar_init(bar(B::kOFinal), 1);
-        mbar_init(bar(B::kVZero), 1);
+        mbar_init(bar(B::kVLand), 1);
         mbar_init(bar(B::kDrain), 1);
         abort_flag = 0;
         no_abort = 0;
@@ -153,18 +158,25 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + wg * T;
         const uint32_t tO = tmem + lane_off + Tr::kTmemO + wg * D;
-        const int ntok_wg = min(tq, it.ntok - wg * tq);  // may be <= 0 for wg 1
-        const int tok = it.tok0 + wg * tq + r / g;
-        const int pos = rq.q_start + tok;
-        const int p_min = rq.q_start + it.tok0 + wg * tq;
-        const int p_max = p_min + ntok_wg - 1;
         const float scale = p.sm_scale_log2;
-        float m_used = -INFINITY;
-        float l = 0.f;
+        uint32_t n_s = 0;  // S_wg tiles consumed so far: the phase of SFull / PFull
+        uint32_t n_o = 0;  // items accumulated into O_wg so far: the phase of OFinal / OEmpty
         bool ok = true;
-        if (wg < nq) {
-            for (int j = 0; j < n_tiles; ++j) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull + wg), j & 1, abort_v, kWaitLimitPP));
+        for (int ii = item_lo; ok && ii < item_hi; ++ii) {
+            const PrefillItem it = p.items[ii];
+            if (wg >= q_tiles(it))
+                continue;
+            const RequestInfo rq = p.reqs[it.req];
+            const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
+            const int ntok_wg = min(tq, it.ntok - wg * tq);
+            const int tok = it.tok0 + wg * tq + r / g;
+            const int pos = rq.q_start + tok;
+            const int p_min = rq.q_start + it.tok0 + wg * tq;
+            const int p_max = p_min + ntok_wg - 1;
+            float m_used = -INFINITY;
+            float l = 0.f;
+            for (int j = 0; j < n_tiles; ++j, ++n_s) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull + wg), n_s & 1, abort_v, kWaitLimitPP));
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -249,48 +261,55 @@ __global__ void __launch_bounds__(384, 1)
                 mbar_arrive(bar(B::kPFull + wg));
             }
             if (ok && n_tiles > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kOFinal), 0, abort_v, kWaitLimitPP));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kOFinal + wg), n_o & 1, abort_v, kWaitLimitPP));
                 tc_fence_after();
             }
-            if (!ok) {
-                record_status(p.status, PKV_ERR_TIMEOUT);
-                abort_flag = 1;
-            } else {
-                const bool row_ok = r < ntok_wg * g;
-                const int h = it.kv_head * g + r % g;
-                const size_t orow = (size_t)(rq.qo_begin + tok) * p.num_qo_heads + h;
-                uint16_t *dst = p.out + orow * D;
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+            if (!ok)
+                break;
+            const bool row_ok = r < ntok_wg * g;
+            const int h = it.kv_head * g + r % g;
+            const size_t orow = (size_t)(rq.qo_begin + tok) * p.num_qo_heads + h;
+            uint16_t *dst = p.out + orow * D;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    if (n_tiles > 0) {
-                        tmem_ld32(tO + 32 * c, o);
-                        tmem_wait_ld();
-                    } else {
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                if (n_tiles > 0) {
+                    tmem_ld32(tO + 32 * c, o);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] = 0.f;
-                    }
-                    if (row_ok) {
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = 0.f;
+                }
+                if (row_ok) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 v;
-                            v.x = pack_bf16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
-                            v.y = pack_bf16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
-                            v.z = pack_bf16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
-                            v.w = pack_bf16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
-                            *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * q4) = v;
-                        }
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 v;
+                        v.x = pack_bf16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
+                        v.y = pack_bf16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+                        v.z = pack_bf16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+                        v.w = pack_bf16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
+                        *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * q4) = v;
                     }
                 }
-                if (row_ok && p.lse)
-                    p.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
             }
+            if (n_tiles > 0) {
+                // O_wg has been read: the next item's first P V may overwrite it.
+                tc_fence_before();
+                mbar_arrive(bar(B::kOEmpty + wg));
+                ++n_o;
+            }
+            if (row_ok && p.lse)
+                p.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        }
+        if (!ok) {
+            record_status(p.status, PKV_ERR_TIMEOUT);
+            abort_flag = 1;
         }
     } else if (warp == 8) {
         // ------------------------------------------------------------ MMA issue
-        // One lane drives everything: waits, MMA issue and commits.
+        // One lane drives everything: Q loads, waits, MMA issue and commits.
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(128, T, false);
             const uint32_t idesc_o = idesc_bf16_f32(128, D, true);
@@ -315,12 +334,46 @@ __global__ void __launch_bounds__(384, 1)
             auto wait = [&](int b_idx, uint32_t parity) {
                 return mbar_wait(bar(b_idx), parity, abort_v, kWaitLimitPP);
             };
+            // Q of an item: its tiles by TMA (4-D map over [token, KV head, group, d]).
+            auto load_q = [&](int ii) {
+                const PrefillItem it = p.items[ii];
+                const int nq = q_tiles(it);
+                const int qo_begin = p.reqs[it.req].qo_begin;
+                const uint32_t rows = (uint32_t)(g * tq);
+                mbar_arrive_expect_tx(bar(B::kQ), (uint32_t)nq * NCH * rows * Tr::kChunk);
+                for (int i = 0; i < nq; ++i)
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_4d(sQ + i * Tr::kQTileBytes + c * (128 * Tr::kChunk), &tm_q, c * 64, 0, it.kv_head,
+                                    qo_begin + it.tok0 + i * tq, bar(B::kQ));
+            };
+            // The next item at or after ii that has KV tiles (items without any
+            // only write zeros and take no part in the pipeline).
+            auto next_busy = [&](int ii) {
+                while (ii < item_hi && p.items[ii].kv_tile_hi <= p.items[ii].kv_tile_lo)
+                    ++ii;
+                return ii;
+            };
+            tma_prefetch_desc(&tm_q);
+            uint32_t n_kv = 0;         // K/V ring position
+            uint32_t n_p[2] = {0, 0};  // P_i tiles consumed: the phase of PFull_i
+            uint32_t n_o[2] = {0, 0};  // items accumulated into O_i: the phase of OEmpty_i
+            uint32_t n_q = 0;          // Q loads: the phase of kQ
             bool ok = true;
-            if (n_tiles > 0) {
-                ok = wait(B::kQ, 0);
-                int sv_prev = 0;
-                for (int j = 0; ok && j < n_tiles; ++j) {
-                    const int nK = 2 * j, nV = 2 * j + 1;
+            int ii = next_busy(item_lo);
+            if (ii < item_hi)
+                load_q(ii);
+            while (ok && ii < item_hi) {
+                const PrefillItem it = p.items[ii];
+                const int nq = q_tiles(it);
+                const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
+                const int ii_next = next_busy(ii + 1);
+                if (!(ok = wait(B::kQ, n_q & 1)))
+                    break;
+                ++n_q;
+                uint32_t sv_prev = 0;
+                for (int j = 0; j < n_tiles; ++j) {
+                    const uint32_t nK = n_kv, nV = n_kv + 1;
+                    n_kv += 2;
                     const int sK = nK % NS, sV = nV % NS;
                     if (!(ok = wait(B::kFull + sK, (nK / NS) & 1)))
                         break;
@@ -329,10 +382,12 @@ __global__ void __launch_bounds__(384, 1)
                     tc_fence_after();
                     issue_s(0, slot(sK));
                     if (j > 0 && nq == 2) {
-                        if (!(ok = wait(B::kPFull + 1, (j - 1) & 1)))
+                        if (!(ok = wait(B::kPFull + 1, n_p[1]++ & 1)))
+                            break;
+                        if (j == 1 && n_o[1] > 0 && !(ok = wait(B::kOEmpty + 1, (n_o[1] - 1) & 1)))
                             break;
                         tc_fence_after();
-                        issue_pv(1, slot(sv_prev), j - 1 == 0);
+                        issue_pv(1, slot(sv_prev), j == 1);
                         umma_commit(bar(B::kEmpty + sv_prev));
                     }
                     if (nq == 2)
@@ -340,29 +395,42 @@ __global__ void __launch_bounds__(384, 1)
                     umma_commit(bar(B::kEmpty + sK));
                     if (!(ok = wait(B::kFull + sV, (nV / NS) & 1)))
                         break;
-                    if (TMA_KV && j == n_tiles - 1 && (it.kv_tile_lo + j) * T + T > rq.kv_len &&
-                        !(ok = wait(B::kVZero, 0)))
-                        break;
                     if (!TMA_KV)
                         fence_proxy_async_smem();
-                    if (!(ok = wait(B::kPFull + 0, j & 1)))
+                    if (!(ok = wait(B::kPFull + 0, n_p[0]++ & 1)))
+                        break;
+                    if (j == 0 && n_o[0] > 0 && !(ok = wait(B::kOEmpty + 0, (n_o[0] - 1) & 1)))
                         break;
                     tc_fence_after();
+                    // Single query tile: S_0 of the last KV tile has been consumed, so
+                    // every read of Q is done and the next item's Q may land.
+                    if (nq == 1 && j == n_tiles - 1 && ii_next < item_hi)
+                        load_q(ii_next);
                     issue_pv(0, slot(sV), j == 0);
                     if (nq == 1)
                         umma_commit(bar(B::kEmpty + sV));
+                    if (j == n_tiles - 1)
+                        umma_commit(bar(B::kOFinal + 0));
                     sv_prev = sV;
                 }
                 if (ok && nq == 2) {
-                    ok = wait(B::kPFull + 1, (n_tiles - 1) & 1);
-                    tc_fence_after();
+                    ok = wait(B::kPFull + 1, n_p[1]++ & 1);
+                    if (ok && n_tiles == 1 && n_o[1] > 0)
+                        ok = wait(B::kOEmpty + 1, (n_o[1] - 1) & 1);
                     if (ok) {
-                        issue_pv(1, slot(sv_prev), n_tiles - 1 == 0);
+                        tc_fence_after();
+                        // S_1 of the last KV tile (issued after S_0) has been consumed.
+                        if (ii_next < item_hi)
+                            load_q(ii_next);
+                        issue_pv(1, slot(sv_prev), n_tiles == 1);
                         umma_commit(bar(B::kEmpty + sv_prev));
+                        umma_commit(bar(B::kOFinal + 1));
                     }
                 }
-                if (ok)
-                    umma_commit(bar(B::kOFinal));
+                ++n_o[0];
+                if (nq == 2)
+                    ++n_o[1];
+                ii = ii_next;
             }
             if (!ok) {
                 record_status(p.status, PKV_ERR_TIMEOUT);
@@ -372,24 +440,27 @@ __global__ void __launch_bounds__(384, 1)
             mbar_wait(bar(B::kDrain), 0, &no_abort, kWaitLimitPP);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ producers
-        const int pw = warp - 9;  // 0..2
-        if (pw == 0 && lane == 0 && n_tiles > 0) {
-            tma_prefetch_desc(&tm_q);
-            const uint32_t rows = (uint32_t)(g * tq);
-            mbar_arrive_expect_tx(bar(B::kQ), (uint32_t)nq * NCH * rows * Tr::kChunk);
-            for (int i = 0; i < nq; ++i)
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_4d(sQ + i * Tr::kQTileBytes + c * (128 * Tr::kChunk), &tm_q, c * 64, 0, it.kv_head,
-                                rq.qo_begin + it.tok0 + i * tq, bar(B::kQ));
-        }
-        if (TMA_KV) {
-            if (pw == 0 && n_tiles > 0) {
-                const int P = p.page_size;
-                const int rows_box = P < T ? P : T;
-                const int npg = T / rows_box;
+    } else if (TMA_KV) {
+        // ------------------------------------------------------------ TMA producer
+        if (warp == 9) {
+            const int P = p.page_size;
+            const int rows_box = P < T ? P : T;
+            const int npg = T / rows_box;
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+            }
+            uint32_t n = 0;       // K/V ring position
+            uint32_t n_land = 0;  // tail V tiles so far: the phase of kVLand
+            bool okp = true;
+            for (int ii = item_lo; okp && ii < item_hi; ++ii) {
+                const PrefillItem it = p.items[ii];
+                const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
+                if (n_tiles <= 0)
+                    continue;
+                const RequestInfo rq = p.reqs[it.req];
                 const int n_pages_req = (rq.kv_len + P - 1) / P;
+                // Lane i: the physical page of the tile's i-th box, or -1.
                 auto load_id = [&](int j) -> int {
                     if (lane >= npg)
                         return -1;
@@ -404,43 +475,41 @@ __global__ void __launch_bounds__(384, 1)
                     }
                     return pg;
                 };
-                if (lane == 0) {
-                    tma_prefetch_desc(&tm_k);
-                    tma_prefetch_desc(&tm_v);
-                }
                 int pg = load_id(0);
-                for (int j = 0; j < n_tiles; ++j) {
+                for (int j = 0; okp && j < n_tiles; ++j) {
                     const int j0 = (it.kv_tile_lo + j) * T;
                     const int slot0 = P > T ? j0 % P : 0;
                     int pg_next = -1;
-                    bool okp = true;
-                    for (int isv = 0; isv < 2; ++isv) {
-                        const int n = 2 * j + isv, s = n % NS;
+                    for (int isv = 0; isv < 2; ++isv, ++n) {
+                        const int s = n % NS;
                         if (n >= NS) {
                             okp = __all_sync(0xffffffffu, mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v,
                                                                     kWaitLimitPP));
                             if (!okp)
                                 break;
                         }
+                        // A V tile reaching past the cache end lands on the producer's
+                        // own barrier: its rows past the end hold stale or foreign data
+                        // and are zeroed (so that P = 0 never meets a non-finite value)
+                        // before the tile is released to the MMA.
+                        const bool tail = isv == 1 && j0 + T > rq.kv_len;
+                        const uint32_t land = tail ? bar(B::kVLand) : bar(B::kFull + s);
                         const unsigned valid = __ballot_sync(0xffffffffu, pg >= 0);
                         if (lane == 0)
-                            mbar_arrive_expect_tx(bar(B::kFull + s),
-                                                  (uint32_t)__popc(valid) * rows_box * Tr::kChunk * NCH);
+                            mbar_arrive_expect_tx(land, (uint32_t)__popc(valid) * rows_box * Tr::kChunk * NCH);
                         __syncwarp();
                         if (pg >= 0) {
                             const void *tm = isv ? (const void *)&tm_v : (const void *)&tm_k;
                             for (int c = 0; c < NCH; ++c)
                                 tma_load_4d(slot(s) + c * (T * Tr::kChunk) + lane * rows_box * Tr::kChunk, tm,
-                                            c * 64, it.kv_head, slot0, pg, bar(B::kFull + s));
+                                            c * 64, it.kv_head, slot0, pg, land);
                         }
                         if (isv == 0 && j + 1 < n_tiles)
                             pg_next = load_id(j + 1);
-                        if (isv == 1 && j == n_tiles - 1 && j0 + T > rq.kv_len) {
-                            // Rows past the end of the cache hold stale or foreign data;
-                            // once the tile has landed, zero them so that P = 0 never
-                            // meets a non-finite value, then release the MMA.
-                            okp = __all_sync(0xffffffffu, mbar_wait(bar(B::kFull + s), (n / NS) & 1, abort_v,
-                                                                    kWaitLimitPP));
+                        if (tail) {
+                            okp = __all_sync(0xffffffffu,
+                                             mbar_wait(bar(B::kVLand), n_land & 1, abort_v, kWaitLimitPP));
+                            ++n_land;
                             if (!okp)
                                 break;
                             const int vr = max(0, rq.kv_len - j0);
@@ -453,30 +522,37 @@ __global__ void __launch_bounds__(384, 1)
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0)
-                                mbar_arrive(bar(B::kVZero));
+                                mbar_arrive(bar(B::kFull + s));
                         }
-                    }
-                    if (!okp) {
-                        if (lane == 0) {
-                            record_status(p.status, PKV_ERR_TIMEOUT);
-                            abort_flag = 1;
-                        }
-                        break;
                     }
                     pg = pg_next;
                 }
             }
-        } else if (n_tiles > 0) {
-            constexpr int NP = Tr::kProducers;
-            const int pt = threadIdx.x - 9 * 32;
-            // Work unit = one row and 8 consecutive 16-byte chunks (one 128-byte
-            // plane row): one page-table lookup feeds 8 copies.
-            constexpr int kUnits = T * (CH / 8);
-            for (int j = 0; j < n_tiles; ++j) {
+            if (!okp && lane == 0) {
+                record_status(p.status, PKV_ERR_TIMEOUT);
+                abort_flag = 1;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ cp.async producers
+        constexpr int NP = Tr::kProducers;
+        const int pt = threadIdx.x - 9 * 32;
+        // Work unit = one row and 8 consecutive 16-byte chunks (one 128-byte
+        // plane row): one page-table lookup feeds 8 copies. Rows past the cache end
+        // are zero-filled.
+        constexpr int kUnits = T * (CH / 8);
+        uint32_t n = 0;  // K/V ring position
+        bool okp = true;
+        for (int ii = item_lo; okp && ii < item_hi; ++ii) {
+            const PrefillItem it = p.items[ii];
+            const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
+            if (n_tiles <= 0)
+                continue;
+            const RequestInfo rq = p.reqs[it.req];
+            for (int j = 0; okp && j < n_tiles; ++j) {
                 const int j0 = (it.kv_tile_lo + j) * T;
-                bool okp = true;
-                for (int isv = 0; isv < 2; ++isv) {
-                    const int n = 2 * j + isv, s = n % NS;
+                for (int isv = 0; isv < 2; ++isv, ++n) {
+                    const int s = n % NS;
                     if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP)) {
                         okp = false;
                         break;
@@ -505,14 +581,13 @@ __global__ void __launch_bounds__(384, 1)
                     }
                     cp_async_mbar_arrive(bar(B::kFull + s));
                 }
-                if (!okp) {
-                    record_status(p.status, PKV_ERR_TIMEOUT);
-                    abort_flag = 1;
-                    break;
-                }
             }
-            asm volatile("cp.async.wait_all;\n" ::: "memory");
         }
+        if (!okp) {
+            record_status(p.status, PKV_ERR_TIMEOUT);
+            abort_flag = 1;
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
     }
 
     tc_fence_before();
@@ -553,7 +628,7 @@ bool encode_4d(CUtensorMap *m, const void *base, const cuuint64_t dims[4], const
 
 template <int D, int MASK, bool TMA_KV>
 cudaError_t launch_pp_dmt(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                          const CUtensorMap &tv, int num_items, cudaStream_t s)
+                          const CUtensorMap &tv, int num_ctas, cudaStream_t s)
 {
     using Tr = PPTraits<D>;
     static bool configured = false;
@@ -564,19 +639,19 @@ cudaError_t launch_pp_dmt(const PrefillParams &p, const CUtensorMap &tq, const C
             return e;
         configured = true;
     }
-    prefill_pp_kernel<D, MASK, TMA_KV><<<num_items, Tr::kThreads, Tr::kDynSmem, s>>>(p, tq, tk, tv);
+    prefill_pp_kernel<D, MASK, TMA_KV><<<num_ctas, Tr::kThreads, Tr::kDynSmem, s>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
 template <int D, bool TMA_KV>
 cudaError_t launch_pp_dt(const PrefillParams &p, int mask_mode, const CUtensorMap &tq, const CUtensorMap &tk,
-                         const CUtensorMap &tv, int num_items, cudaStream_t s)
+                         const CUtensorMap &tv, int num_ctas, cudaStream_t s)
 {
     switch (mask_mode) {
-    case kMaskNone: return launch_pp_dmt<D, kMaskNone, TMA_KV>(p, tq, tk, tv, num_items, s);
-    case kMaskCausal: return launch_pp_dmt<D, kMaskCausal, TMA_KV>(p, tq, tk, tv, num_items, s);
-    case kMaskCausalWindow: return launch_pp_dmt<D, kMaskCausalWindow, TMA_KV>(p, tq, tk, tv, num_items, s);
-    case kMaskWindow: return launch_pp_dmt<D, kMaskWindow, TMA_KV>(p, tq, tk, tv, num_items, s);
+    case kMaskNone: return launch_pp_dmt<D, kMaskNone, TMA_KV>(p, tq, tk, tv, num_ctas, s);
+    case kMaskCausal: return launch_pp_dmt<D, kMaskCausal, TMA_KV>(p, tq, tk, tv, num_ctas, s);
+    case kMaskCausalWindow: return launch_pp_dmt<D, kMaskCausalWindow, TMA_KV>(p, tq, tk, tv, num_ctas, s);
+    case kMaskWindow: return launch_pp_dmt<D, kMaskWindow, TMA_KV>(p, tq, tk, tv, num_ctas, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -593,7 +668,7 @@ bool prefill_pp_tma_page_size(int page_size, int head_dim)
 
 int prefill_kv_tile(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 
-cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mode, int num_items, cudaStream_t s)
+cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mode, int num_ctas, cudaStream_t s)
 {
     const int g = p.group, tq = p.tokens_per_tile, Hkv = p.num_kv_heads, P = p.page_size;
     const bool tma_kv = prefill_pp_tma_page_size(P, head_dim);
@@ -619,14 +694,14 @@ cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mod
     }
     switch (head_dim) {
     case 64:
-        return tma_kv ? launch_pp_dt<64, true>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s)
-                      : launch_pp_dt<64, false>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s);
+        return tma_kv ? launch_pp_dt<64, true>(p, mask_mode, tm_q, tm_k, tm_v, num_ctas, s)
+                      : launch_pp_dt<64, false>(p, mask_mode, tm_q, tm_k, tm_v, num_ctas, s);
     case 128:
-        return tma_kv ? launch_pp_dt<128, true>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s)
-                      : launch_pp_dt<128, false>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s);
+        return tma_kv ? launch_pp_dt<128, true>(p, mask_mode, tm_q, tm_k, tm_v, num_ctas, s)
+                      : launch_pp_dt<128, false>(p, mask_mode, tm_q, tm_k, tm_v, num_ctas, s);
     case 256:
-        return tma_kv ? launch_pp_dt<256, true>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s)
-                      : launch_pp_dt<256, false>(p, mask_mode, tm_q, tm_k, tm_v, num_items, s);
+        return tma_kv ? launch_pp_dt<256, true>(p, mask_mode, tm_q, tm_k, tm_v, num_ctas, s)
+                      : launch_pp_dt<256, false>(p, mask_mode, tm_q, tm_k, tm_v, num_ctas, s);
     default: return cudaErrorInvalidValue;
     }
 }
