@@ -325,8 +325,14 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
                     tlo = (int32_t)(lo / T);
                     thi = (int32_t)(hi / T + 1);
                 }
+                // Start tile: the query block's index times the golden ratio,
+                // modulo the tile count, so that neighbouring blocks (which run at
+                // the same time over nearly the same KV tiles) start far apart.
+                const int32_t ntl = thi - tlo;
+                const double frac = std::fmod((double)(t0 / tq) * 0.6180339887498949, 1.0);
+                const int32_t rot = ntl > 1 ? std::min<int32_t>(ntl - 1, (int32_t)(frac * ntl)) : 0;
                 for (int hk = 0; hk < d.num_kv_heads; ++hk)
-                    p_items.push_back({b, hk, (int32_t)t0, (int32_t)nt, tlo, thi, 0, 0});
+                    p_items.push_back({b, hk, (int32_t)t0, (int32_t)nt, tlo, thi, rot, 0});
             }
         }
         // Persistent CTAs, one per SM: longest-processing-time-first assignment of

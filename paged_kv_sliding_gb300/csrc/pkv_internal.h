@@ -31,8 +31,19 @@ struct PrefillItem {
     int32_t ntok;        // query tokens in the tile
     int32_t kv_tile_lo;  // first KV tile (in units of the kernel's KV tile)
     int32_t kv_tile_hi;  // one past the last KV tile
-    int32_t pad0, pad1;
+    int32_t kv_tile_rot; // tiles are visited from kv_tile_lo + kv_tile_rot, wrapping around
+    int32_t pad0;
 };
+
+// The KV tile visited at step j (0 <= j < hi - lo) of a prefill item. Softmax
+// accumulation is order-independent; staggering the start keeps the items that
+// run at the same time on one KV head from all missing L2 on the same tile.
+__host__ __device__ inline int prefill_kv_tile_at(const PrefillItem &it, int j)
+{
+    const int n = it.kv_tile_hi - it.kv_tile_lo;
+    const int k = j + it.kv_tile_rot;
+    return it.kv_tile_lo + (k < n ? k : k - n);
+}
 
 // One CTA of the decode kernel: up to kDecodeRows query heads of one request's
 // single row against the key range [j0, j1) of one KV head.

@@ -53,12 +53,15 @@ struct PPTraits {
     static constexpr int kDynSmem = kOffSlots + kSlots * kSlotBytes + 1024;
     static constexpr int kThreads = 384;
     static constexpr int kProducers = 96;     // cp.async mode: warps 9-11
+    static constexpr int kIdsPerTile = kT;    // page-id ring entries per tile (one per row)
     static constexpr int kTmemCols = 512;
     static constexpr int kTmemO = 256;        // O_i at kTmemO + i * D; S_i at i * kT
     static_assert(kTmemO + kNQ * D <= kTmemCols && kNQ * kT <= kTmemO, "TMEM budget");
 };
 
 constexpr long long kWaitLimitPP = 4000000000LL;
+// Page-id ring of the cp.async producers, in tiles (ids of kIdRing - 1 tiles in flight).
+constexpr int kIdRing = 3;
 constexpr int kRegsLaunch = 168;   // 65536 / 384 rounded down to a multiple of 8
 constexpr int kRegsSoftmax = 200;
 constexpr int kRegsOther = 96;
@@ -97,6 +100,7 @@ __global__ void __launch_bounds__(384, 1)
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_flag;
     __shared__ int no_abort;
+    __shared__ int id_ring[TMA_KV ? 1 : kIdRing * Tr::kIdsPerTile];
 
     const uint32_t base = (smem_u32(dsmem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = base + Tr::kOffQ;
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(384, 1)
                     tmem_ld32(tS + 32 * c, *reinterpret_cast<float(*)[32]>(&s[32 * c]));
                 tmem_wait_ld();
 
-                const int j0 = (it.kv_tile_lo + j) * T;
+                const int j0 = prefill_kv_tile_at(it, j) * T;
                 bool need_mask = j0 + T > rq.kv_len;
                 if (kCausal)
                     need_mask |= j0 + T - 1 > p_min;
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(384, 1)
                 auto load_id = [&](int j) -> int {
                     if (lane >= npg)
                         return -1;
-                    const int j0 = (it.kv_tile_lo + j) * T;
+                    const int j0 = prefill_kv_tile_at(it, j) * T;
                     const int lp = P <= T ? j0 / P + lane : j0 / P;
                     if (lp >= n_pages_req)
                         return -1;
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(384, 1)
                 };
                 int pg = load_id(0);
                 for (int j = 0; okp && j < n_tiles; ++j) {
-                    const int j0 = (it.kv_tile_lo + j) * T;
+                    const int j0 = prefill_kv_tile_at(it, j) * T;
                     const int slot0 = P > T ? j0 % P : 0;
                     int pg_next = -1;
                     for (int isv = 0; isv < 2; ++isv, ++n) {
@@ -539,18 +543,63 @@ __global__ void __launch_bounds__(384, 1)
         const int pt = threadIdx.x - 9 * 32;
         // Work unit = one row and 8 consecutive 16-byte chunks (one 128-byte
         // plane row): one page-table lookup feeds 8 copies. Rows past the cache end
-        // are zero-filled.
+        // are zero-filled. The page id of every row is fetched kIdRing - 1 tiles
+        // ahead into the shared ring by cp.async (the producers never stall on a
+        // page-table read); named barrier 1 orders the ring among the producers.
         constexpr int kUnits = T * (CH / 8);
-        uint32_t n = 0;  // K/V ring position
+        int c_ii = item_lo, c_j = 0, c_at = -1;
+        PrefillItem c_it{};
+        int c_kv_len = 0, c_page_begin = 0;
+        uint32_t n_ids = 0;
+        auto fetch_ids = [&]() {
+            while (c_ii < item_hi) {
+                if (c_at != c_ii) {
+                    c_it = p.items[c_ii];
+                    const RequestInfo r = p.reqs[c_it.req];
+                    c_kv_len = r.kv_len;
+                    c_page_begin = r.kv_page_begin;
+                    c_at = c_ii;
+                }
+                if (c_j < c_it.kv_tile_hi - c_it.kv_tile_lo)
+                    break;
+                ++c_ii;
+                c_j = 0;
+            }
+            if (c_ii < item_hi) {
+                const int j0 = prefill_kv_tile_at(c_it, c_j) * T;
+                for (int t = pt; t < T; t += NP) {
+                    int *dst = &id_ring[(n_ids % kIdRing) * Tr::kIdsPerTile + t];
+                    const int jj = j0 + t;
+                    if (jj < c_kv_len) {
+                        const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
+                        cp_async_4(smem_u32(dst), p.kv_indices + c_page_begin + lp);
+                    } else {
+                        *dst = -1;
+                    }
+                }
+            }
+            cp_async_commit();
+            ++c_j;
+            ++n_ids;
+        };
+        auto sync_producers = [] { asm volatile("bar.sync 1, %0;\n" ::"n"(Tr::kProducers) : "memory"); };
+        for (int k = 0; k < kIdRing - 1; ++k)
+            fetch_ids();
+        uint32_t n = 0;    // K/V ring position
+        uint32_t n_t = 0;  // tiles gathered so far
         bool okp = true;
         for (int ii = item_lo; okp && ii < item_hi; ++ii) {
             const PrefillItem it = p.items[ii];
             const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
             if (n_tiles <= 0)
                 continue;
-            const RequestInfo rq = p.reqs[it.req];
-            for (int j = 0; okp && j < n_tiles; ++j) {
-                const int j0 = (it.kv_tile_lo + j) * T;
+            for (int j = 0; okp && j < n_tiles; ++j, ++n_t) {
+                const int j0 = prefill_kv_tile_at(it, j) * T;
+                sync_producers();  // every producer is done with the ring entry refilled next
+                fetch_ids();
+                cp_async_wait<kIdRing - 1>();
+                sync_producers();  // this tile's ids are visible to all producers
+                const int *ids = &id_ring[(n_t % kIdRing) * Tr::kIdsPerTile];
                 for (int isv = 0; isv < 2; ++isv, ++n) {
                     const int s = n % NS;
                     if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP)) {
@@ -561,13 +610,13 @@ __global__ void __launch_bounds__(384, 1)
                     for (int u = pt; u < kUnits; u += NP) {
                         const int t = u / (CH / 8), pl = u % (CH / 8);  // row, 64-column plane
                         const int jj = j0 + t;
+                        const int page = ids[t];
                         size_t off = 0;
                         uint32_t bytes = 0;
-                        if (jj < rq.kv_len) {
-                            const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
-                            const int sl = jj - lp * p.page_size;
-                            const int page = __ldg(p.kv_indices + rq.kv_page_begin + lp);
+                        if (page >= 0) {
                             if ((unsigned)page < (unsigned)p.num_pages) {
+                                const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
+                                const int sl = jj - lp * p.page_size;
                                 off = (((size_t)page * p.page_size + sl) * p.num_kv_heads + it.kv_head) * D + pl * 64;
                                 bytes = 16;
                             } else {

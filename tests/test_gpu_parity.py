@@ -122,6 +122,23 @@ def test_extend_with_prefix_sampled(pkv, oracle_lib):
     check(pkv, oracle_lib, w, rows=np.array(rows))
 
 
+@pytest.mark.parametrize("d,P,W", [(128, 16, 1023), (128, 64, -1), (128, 256, 300), (256, 16, 511),
+                                   (256, 128, -1), (128, 1, 700)])
+def test_prefill_persistent_many_items(pkv, oracle_lib, d, P, W):
+    """Several work items per persistent CTA, each walking its KV tiles from a
+    staggered start tile (wrapping around): one- and two-tile items, tail tiles
+    past the cache end, pages larger than a KV tile; every row against the oracle."""
+    rng = np.random.default_rng(d + P)
+    n = 16
+    qo = rng.integers(40, 420, size=n)
+    qo[0], qo[1] = 1, 33
+    kv = qo + rng.integers(0, 900, size=n)
+    w = wl.make_workload(name="many", qo_lens=qo, kv_lens=kv, num_qo_heads=32, num_kv_heads=8,
+                         head_dim=d, page_size=P, window_left=W, causal=True, seed=7 * d + P)
+    _, info = check(pkv, oracle_lib, w)
+    assert info["num_work_items"] > 2 * 152, info
+
+
 def test_extend_prefix_split_merge(pkv, oracle_lib):
     """KV split at the page boundary floor(prefix/16)*16 into two plans (the prefix
     plan with q_start so its rows keep their true positions), merged by
