@@ -62,6 +62,14 @@ struct PPTraits {
 constexpr long long kWaitLimitPP = 4000000000LL;
 // Page-id ring of the cp.async producers, in tiles (ids of kIdRing - 1 tiles in flight).
 constexpr int kIdRing = 3;
+
+// K and V of a KV tile complete one barrier, the K slot's: a slot's barrier then
+// completes one phase per use of the slot as a K slot. K tiles sit at the even
+// ring positions, so with an even slot count every use of an even slot is a K use
+// (a phase every NS positions) and with an odd count every other use is (a phase
+// every 2 NS positions).
+template <int NS>
+__host__ __device__ constexpr int full_period() { return NS % 2 == 0 ? NS : 2 * NS; }
 constexpr int kRegsLaunch = 168;   // 65536 / 384 rounded down to a multiple of 8
 constexpr int kRegsSoftmax = 200;
 constexpr int kRegsOther = 96;
@@ -70,7 +78,7 @@ static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * kRegsLaunch, "regis
 template <int NS>
 struct PPBars {
     static constexpr int kQ = 0;
-    static constexpr int kFull = 1;
+    static constexpr int kFull = 1;              // NS: K and V of a tile landed (on the K slot's barrier)
     static constexpr int kEmpty = kFull + NS;
     static constexpr int kSFull = kEmpty + NS;   // 2: S_i(j) complete in TMEM
     static constexpr int kPFull = kSFull + 2;    // 2: P_i(j) written to TMEM (128 arrivals)
@@ -89,6 +97,7 @@ __global__ void __launch_bounds__(384, 1)
     using Tr = PPTraits<D>;
     constexpr int NS = Tr::kSlots;
     using B = PPBars<NS>;
+    constexpr int kFullPeriod = full_period<NS>();
     constexpr int T = Tr::kT;
     constexpr int NCH = Tr::kNCh;
     constexpr int CH = D / 8;
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(384, 1)
                     const uint32_t nK = n_kv, nV = n_kv + 1;
                     n_kv += 2;
                     const int sK = nK % NS, sV = nV % NS;
-                    if (!(ok = wait(B::kFull + sK, (nK / NS) & 1)))
+                    if (!(ok = wait(B::kFull + sK, (nK / kFullPeriod) & 1)))
                         break;
                     if (!TMA_KV)
                         fence_proxy_async_smem();
@@ -397,10 +406,6 @@ __global__ void __launch_bounds__(384, 1)
                     if (nq == 2)
                         issue_s(1, slot(sK));
                     umma_commit(bar(B::kEmpty + sK));
-                    if (!(ok = wait(B::kFull + sV, (nV / NS) & 1)))
-                        break;
-                    if (!TMA_KV)
-                        fence_proxy_async_smem();
                     if (!(ok = wait(B::kPFull + 0, n_p[0]++ & 1)))
                         break;
                     if (j == 0 && n_o[0] > 0 && !(ok = wait(B::kOEmpty + 0, (n_o[0] - 1) & 1)))
@@ -484,6 +489,15 @@ __global__ void __launch_bounds__(384, 1)
                     const int j0 = prefill_kv_tile_at(it, j) * T;
                     const int slot0 = P > T ? j0 % P : 0;
                     int pg_next = -1;
+                    // K, then V. Both complete the K slot's barrier; a V tile reaching
+                    // past the cache end lands on the producer's own barrier instead:
+                    // its rows past the end hold stale or foreign data and are zeroed
+                    // (so that P = 0 never meets a non-finite value) before the
+                    // producer's arrival completes the K slot's barrier.
+                    const bool tail = j0 + T > rq.kv_len;
+                    const unsigned valid = __ballot_sync(0xffffffffu, pg >= 0);
+                    const uint32_t bytes = (uint32_t)__popc(valid) * rows_box * Tr::kChunk * NCH;
+                    const uint32_t full = bar(B::kFull + n % NS);
                     for (int isv = 0; isv < 2; ++isv, ++n) {
                         const int s = n % NS;
                         if (n >= NS) {
@@ -492,15 +506,16 @@ __global__ void __launch_bounds__(384, 1)
                             if (!okp)
                                 break;
                         }
-                        // A V tile reaching past the cache end lands on the producer's
-                        // own barrier: its rows past the end hold stale or foreign data
-                        // and are zeroed (so that P = 0 never meets a non-finite value)
-                        // before the tile is released to the MMA.
-                        const bool tail = isv == 1 && j0 + T > rq.kv_len;
-                        const uint32_t land = tail ? bar(B::kVLand) : bar(B::kFull + s);
-                        const unsigned valid = __ballot_sync(0xffffffffu, pg >= 0);
-                        if (lane == 0)
-                            mbar_arrive_expect_tx(land, (uint32_t)__popc(valid) * rows_box * Tr::kChunk * NCH);
+                        const bool vtail = isv == 1 && tail;
+                        const uint32_t land = vtail ? bar(B::kVLand) : full;
+                        if (lane == 0) {
+                            if (isv == 0 && tail)
+                                mbar_expect_tx(full, bytes);  // the arrival comes after the zeroing
+                            else if (isv == 0)
+                                mbar_arrive_expect_tx(full, 2 * bytes);
+                            else if (vtail)
+                                mbar_arrive_expect_tx(land, bytes);
+                        }
                         __syncwarp();
                         if (pg >= 0) {
                             const void *tm = isv ? (const void *)&tm_v : (const void *)&tm_k;
@@ -510,7 +525,7 @@ __global__ void __launch_bounds__(384, 1)
                         }
                         if (isv == 0 && j + 1 < n_tiles)
                             pg_next = load_id(j + 1);
-                        if (tail) {
+                        if (vtail) {
                             okp = __all_sync(0xffffffffu,
                                              mbar_wait(bar(B::kVLand), n_land & 1, abort_v, kWaitLimitPP));
                             ++n_land;
@@ -526,7 +541,7 @@ __global__ void __launch_bounds__(384, 1)
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0)
-                                mbar_arrive(bar(B::kFull + s));
+                                mbar_arrive(full);
                         }
                     }
                     pg = pg_next;
@@ -600,6 +615,7 @@ __global__ void __launch_bounds__(384, 1)
                 cp_async_wait<kIdRing - 1>();
                 sync_producers();  // this tile's ids are visible to all producers
                 const int *ids = &id_ring[(n_t % kIdRing) * Tr::kIdsPerTile];
+                const uint32_t full = bar(B::kFull + n % NS);  // K and V of the tile complete it
                 for (int isv = 0; isv < 2; ++isv, ++n) {
                     const int s = n % NS;
                     if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP)) {
@@ -628,7 +644,8 @@ __global__ void __launch_bounds__(384, 1)
                         for (int c = 0; c < 8; ++c)
                             cp_async_16(row_base + ((c ^ (t & 7)) << 4), src + off + c * 8, bytes);
                     }
-                    cp_async_mbar_arrive(bar(B::kFull + s));
+                    if (isv == 1)
+                        cp_async_mbar_arrive(full);
                 }
             }
         }
