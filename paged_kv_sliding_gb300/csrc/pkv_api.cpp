@@ -57,6 +57,7 @@ struct pkv_plan {
     int num_partials = 0;
     int num_merge_items = 0;
     int num_ctas = 0;  // prefill: persistent CTAs
+    int decode_tile = 64;  // decode: KV tokens per stage of the kernel
     int64_t total_q = 0;
     const int32_t *kv_indices = nullptr;  // borrowed device pointer
     void *workspace = nullptr;
@@ -306,6 +307,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     std::vector<DecodeItem> d_items;
     std::vector<MergeItem> m_items;
     std::vector<int32_t> cta_items;  // prefill: per-CTA item offsets
+    int decode_tile = 64;
     int num_partials = 0;
     int num_counters = 0;
     int mask_mode = causal ? (W >= 0 ? kMaskCausalWindow : kMaskCausal)
@@ -411,12 +413,14 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
                         d_items.push_back({b, hk, hk * group + h0, std::min(kDecodeRows, group - h0),
                                            (int32_t)j0, (int32_t)j1, n > 1 ? (int32_t)(pbase + s) : -1,
                                            pbase, (int32_t)n,
-                                           n > 1 ? cbase + hk * head_blocks + h0 / kDecodeRows : -1, 0, 0});
+                                           n > 1 ? cbase + hk * head_blocks + h0 / kDecodeRows : -1,
+                                           h_reqs[b].qo_begin, h_reqs[b].kv_len, h_reqs[b].kv_page_begin, 0});
             }
         }
         std::stable_sort(d_items.begin(), d_items.end(), [](const DecodeItem &a, const DecodeItem &b) {
             return (a.j1 - a.j0) > (b.j1 - b.j0);
         });
+        decode_tile = decode_tile_for(d.head_dim, d_items.empty() ? 0 : d_items.front().j1 - d_items.front().j0);
     }
 
     // One device workspace: requests | items | merge items | partial o | partial lse | status.
@@ -478,6 +482,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     plan->num_partials = num_partials;
     plan->num_merge_items = (int)m_items.size();
     plan->num_ctas = cta_items.empty() ? 0 : (int)cta_items.size() - 1;
+    plan->decode_tile = decode_tile;
     plan->total_q = total_q;
     plan->kv_indices = d.kv_indices;
     plan->workspace_bytes = ws_bytes;
@@ -600,7 +605,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
         p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
         if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
             return cuda_fail(ce, "cudaEventRecord");
-        ce = launch_decode(p, d.head_dim, plan->num_items, stream);
+        ce = launch_decode(p, d.head_dim, plan->num_items, stream, plan->decode_tile);
         if (ce != cudaSuccess)
             return cuda_fail(ce, "decode kernel launch");
         if (plan->ev_end && (ce = cudaEventRecord(plan->ev_end, stream)) != cudaSuccess)

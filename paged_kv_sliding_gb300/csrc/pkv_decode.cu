@@ -8,12 +8,13 @@
 // the range is visible; the kernel masks only what lies outside it in the first
 // and last 64-token tile.
 //
-// CTA = 4 compute warps + 1 producer warp (160 threads):
-//   producer: fills a ring of shared-memory stages (64 tokens of K and of V each,
+// CTA = TT/16 compute warps + 1 producer warp, TT = 64 tokens per stage (160
+// threads) or, for batches of short key ranges, 32 (96 threads, 4 CTAs per SM):
+//   producer: fills a ring of shared-memory stages (TT tokens of K and of V each,
 //     stored as 128-byte-swizzled 64-column planes) either with TMA boxes of whole
 //     pages (a 4-D tensor map over [page, slot, KV head, d]; the page ids of the
 //     next tile are fetched while the current one is issued) when the page size
-//     is a multiple of 8 that divides 64 or is a multiple of it, or else with
+//     is a multiple of 8 that divides TT or is a multiple of it, or else with
 //     16-byte cp.async gathers; completion through mbarriers;
 //   compute warp w: tokens [16w, 16w + 16) of every tile, S = Q K^T and O += P V
 //     with mma.sync m16n8k16 (bf16 in, fp32 accumulate, rows = the query heads),
@@ -32,46 +33,51 @@
 namespace pkv {
 namespace {
 
-template <int D>
+// TT = KV tokens per stage: 64 (the general kernel, 2 CTAs per SM at d <= 128) or
+// 32 for batches of short key ranges (two compute warps and a 48 KB ring at d 128,
+// 4 CTAs per SM, so that a batch of short ranges runs in one wave).
+template <int D, int TT>
 struct DecTraits {
-    static constexpr int kTile = 64;        // KV tokens per stage
-    static constexpr int kCompute = 4;      // compute warps
-    static constexpr int kThreads = 160;    // + one producer warp
+    static constexpr int kTile = TT;
+    static constexpr int kCompute = TT / 16;  // compute warps, 16 tokens of each tile apiece
+    static constexpr int kThreads = 32 * (kCompute + 1);  // + one producer warp
     static constexpr int kNCh = D / 64;     // 128-byte column planes
     static constexpr int kPlaneBytes = kTile * 128;
     static constexpr int kTileBytes = kTile * D * 2;  // K or V of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kStages = D == 64 ? 4 : 3;
     static constexpr int kORowFloats = D + 8;  // padded row of the combine buffer
-    static constexpr int kCombineBytes = 4 * kDecodeRows * kORowFloats * 4;
+    static constexpr int kCombineBytes = kCompute * kDecodeRows * kORowFloats * 4;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kDynSmem = (kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes) + 1024;
-    static constexpr int kMinBlocks = D >= 256 ? 1 : 2;
+    static constexpr int kMinBlocks = TT == 32 ? 4 : (D >= 256 ? 1 : 2);
 };
 
 constexpr long long kDecWaitLimit = 4000000000LL;
 
-// Byte offset of 16-byte granule `c16` (0 .. D/8-1) of row `row` in a tile stored
-// as 64-column planes of 128-byte rows with the 128-byte XOR swizzle (the layout
-// a SWIZZLE_128B TMA box produces).
+// Byte offset of 16-byte granule `c16` (0 .. D/8-1) of row `row` in a TT-row tile
+// stored as 64-column planes of 128-byte rows with the 128-byte XOR swizzle (the
+// layout a SWIZZLE_128B TMA box produces).
+template <int TT>
 __device__ __forceinline__ uint32_t plane_off(int row, int c16)
 {
-    return (uint32_t)((c16 >> 3) * (64 * 128) + row * 128 + (((c16 & 7) ^ (row & 7)) << 4));
+    return (uint32_t)((c16 >> 3) * (TT * 128) + row * 128 + (((c16 & 7) ^ (row & 7)) << 4));
 }
 
-template <int D, bool TMA_KV>
-__global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
+template <int D, bool TMA_KV, int TT>
+__global__ void __launch_bounds__(DecTraits<D, TT>::kThreads, DecTraits<D, TT>::kMinBlocks)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v)
 {
-    using Tr = DecTraits<D>;
+    using Tr = DecTraits<D, TT>;
     constexpr int S = Tr::kStages;
-    constexpr int TT = Tr::kTile;
+    constexpr int NW = Tr::kCompute;
+    constexpr int NT = 32 * NW;  // compute threads
     extern __shared__ uint8_t dsmem_raw[];
     __shared__ __align__(8) uint64_t full_bar[S];
     __shared__ __align__(8) uint64_t empty_bar[S];
-    __shared__ float red_m[4][kDecodeRows];
-    __shared__ float red_l[4][kDecodeRows];
+    __shared__ float red_m[NW][kDecodeRows];
+    __shared__ float red_l[NW][kDecodeRows];
     __shared__ float row_m[kDecodeRows];
     __shared__ float row_inv_l[kDecodeRows];
     __shared__ int abort_flag;
@@ -83,7 +89,9 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const DecodeItem it = p.items[blockIdx.x];
-    const RequestInfo rq = p.reqs[it.req];
+    struct {
+        int32_t qo_begin, kv_len, kv_page_begin;
+    } const rq = {it.row, it.kv_len, it.kv_page_begin};
     const int tb = it.j1 > it.j0 ? (it.j0 / TT) * TT : it.j0;  // first tile start (64-aligned)
     const int ntiles = it.j1 > it.j0 ? (it.j1 - tb + TT - 1) / TT : 0;
     const volatile int *abort_v = &abort_flag;
@@ -189,8 +197,8 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
                     }
 #pragma unroll
                     for (int c = 0; c < CH; ++c) {
-                        cp_async_16(kb + plane_off(row, c), p.k_cache + off + c * 8, bytes);
-                        cp_async_16(vb + plane_off(row, c), p.v_cache + off + c * 8, bytes);
+                        cp_async_16(kb + plane_off<TT>(row, c), p.k_cache + off + c * 8, bytes);
+                        cp_async_16(vb + plane_off<TT>(row, c), p.v_cache + off + c * 8, bytes);
                     }
                 }
                 cp_async_mbar_arrive(smem_u32(&full_bar[s]));
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
                     const int row = warp * 16 + e / (D / 8), c = e % (D / 8);
                     const int j = tb + t * TT + row;
                     if (j < it.j0 || j >= it.j1)
-                        *reinterpret_cast<uint4 *>(vgen + plane_off(row, c)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vgen + plane_off<TT>(row, c)) = make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
             }
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
                 const int row = warp * 16 + ((mi >> 1) << 3) + (lane & 7);
                 const int c16 = 2 * ks + (mi & 1);
                 uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(kb + plane_off(row, c16), b0, b1, b2, b3);
+                ldmatrix_x4(kb + plane_off<TT>(row, c16), b0, b1, b2, b3);
                 mma_bf16_16816(sc[0], qf[ks], b0, b1);
                 mma_bf16_16816(sc[1], qf[ks], b2, b3);
             }
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
                 const int row = warp * 16 + ((mi & 1) << 3) + (lane & 7);
                 const int c16 = 2 * np + (mi >> 1);
                 uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(vb + plane_off(row, c16), b0, b1, b2, b3);
+                ldmatrix_x4_trans(vb + plane_off<TT>(row, c16), b0, b1, b2, b3);
                 mma_bf16_16816(o[2 * np], pa, b0, b1);
                 mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
             }
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
             abort_flag = 1;
         }
 
-        // Merge the four warps' states (named barrier over the 128 compute threads).
+        // Merge the compute warps' states (named barrier 1 over the compute threads).
         l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
         l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
         l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
@@ -340,13 +348,16 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
             red_l[warp][r0] = l[0];
             red_l[warp][r1] = l[1];
         }
-        asm volatile("bar.sync 1, 128;\n" ::: "memory");
+        asm volatile("bar.sync 1, %0;\n" ::"n"(NT) : "memory");
         if (tid < kDecodeRows) {
-            const float M = fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]), fmaxf(red_m[2][tid], red_m[3][tid]));
+            float M = red_m[0][tid];
+#pragma unroll
+            for (int w = 1; w < NW; ++w)
+                M = fmaxf(M, red_m[w][tid]);
             const float ref = M == -INFINITY ? 0.f : M;
             float L = 0.f;
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
+            for (int w = 0; w < NW; ++w)
                 L += red_l[w][tid] * fast_exp2(red_m[w][tid] - ref);
             row_m[tid] = M;
             row_inv_l[tid] = L > 0.f ? 1.f / L : 0.f;
@@ -362,7 +373,7 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
         // Every stage has been consumed (or the CTA is aborting): the ring holds no
         // copy in flight that is still needed and becomes the combine buffer once
         // all compute warps passed their last tile.
-        asm volatile("bar.sync 1, 128;\n" ::: "memory");
+        asm volatile("bar.sync 1, %0;\n" ::"n"(NT) : "memory");
         float *sO = reinterpret_cast<float *>(ring_gen);
         {
             const float M0 = row_m[r0], M1 = row_m[r1];
@@ -376,9 +387,9 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
                 *reinterpret_cast<float2 *>(w1 + 8 * i) = make_float2(o[i][2] * f1, o[i][3] * f1);
             }
         }
-        asm volatile("bar.sync 1, 128;\n" ::: "memory");
+        asm volatile("bar.sync 1, %0;\n" ::"n"(NT) : "memory");
         if (!abort_flag) {
-            for (int idx = tid; idx < kDecodeRows * (D / 8); idx += 128) {
+            for (int idx = tid; idx < kDecodeRows * (D / 8); idx += NT) {
                 const int r = idx / (D / 8);
                 const int c = (idx % (D / 8)) * 8;
                 if (r >= it.nheads)
@@ -388,7 +399,7 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
                 for (int e = 0; e < 8; ++e)
                     acc[e] = 0.f;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
+                for (int w = 0; w < NW; ++w) {
                     const float4 *src =
                         reinterpret_cast<const float4 *>(sO + (w * kDecodeRows + r) * Tr::kORowFloats + c);
                     const float4 x = src[0], y = src[1];
@@ -416,16 +427,17 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
             // finish merges the group's partial states through their LSE (the
             // merge_state of flashinfer_backend.py, n-way) and re-arms the counter.
             __shared__ int last_flag;
-            asm volatile("bar.sync 1, 128;\n" ::: "memory");  // this CTA's partials are written
+            asm volatile("bar.sync 1, %0;\n" ::"n"(NT) : "memory");  // this CTA's partials are written
             if (tid == 0) {
                 __threadfence();
                 last_flag = atomicAdd(p.merge_counters + it.counter, 1) == it.nsplit - 1;
             }
-            asm volatile("bar.sync 1, 128;\n" ::: "memory");
+            asm volatile("bar.sync 1, %0;\n" ::"n"(NT) : "memory");
             if (last_flag) {
                 __threadfence();
                 constexpr int CPT = D / 8;  // columns per thread: 8 threads per head
-                const int r = tid >> 3, c0 = (tid & 7) * CPT;
+                for (int idx = tid; idx < kDecodeRows * 8; idx += NT) {
+                const int r = idx >> 3, c0 = (idx & 7) * CPT;
                 if (r < it.nheads) {
                     const int h = it.head0 + r;
                     float mx = -INFINITY;
@@ -463,9 +475,10 @@ __global__ void __launch_bounds__(160, DecTraits<D>::kMinBlocks)
                         v.w = pack_bf16(acc[8 * q8 + 6] * inv, acc[8 * q8 + 7] * inv);
                         reinterpret_cast<uint4 *>(dst)[q8] = v;
                     }
-                    if (p.lse && (tid & 7) == 0)
+                    if (p.lse && (idx & 7) == 0)
                         p.lse[(size_t)rq.qo_begin * p.num_qo_heads + h] =
                             sum > 0.f ? mx + __log2f(sum) * 0.6931471805599453f : -INFINITY;
+                }
                 }
                 if (tid == 0)
                     atomicExch(p.merge_counters + it.counter, 0);
@@ -498,20 +511,20 @@ bool encode_kv_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_he
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool TMA_KV>
+template <int D, bool TMA_KV, int TT>
 cudaError_t launch_decode_dt(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int num_items,
                              cudaStream_t s)
 {
-    using Tr = DecTraits<D>;
+    using Tr = DecTraits<D, TT>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, TMA_KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Tr::kDynSmem);
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, TMA_KV, TT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kDynSmem);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    decode_kernel<D, TMA_KV><<<num_items, Tr::kThreads, Tr::kDynSmem, s>>>(p, tk, tv);
+    decode_kernel<D, TMA_KV, TT><<<num_items, Tr::kThreads, Tr::kDynSmem, s>>>(p, tk, tv);
     return cudaGetLastError();
 }
 
@@ -524,23 +537,34 @@ bool decode_tma_page_size(int page_size)
     return page_size <= 64 ? 64 % page_size == 0 : page_size % 64 == 0;
 }
 
-cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s)
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile)
 {
     const bool tma = decode_tma_page_size(p.page_size);
+    if (tile == 32 && head_dim > 128)
+        return cudaErrorInvalidValue;
     CUtensorMap tk{}, tv{};
     if (tma) {
-        const int rows = p.page_size < 64 ? p.page_size : 64;
+        const int rows = p.page_size < tile ? p.page_size : tile;
         if (!encode_kv_map(&tk, p.k_cache, head_dim, p.num_kv_heads, p.page_size, p.num_pages, rows) ||
             !encode_kv_map(&tv, p.v_cache, head_dim, p.num_kv_heads, p.page_size, p.num_pages, rows))
             return cudaErrorInvalidValue;
     }
+    if (tile == 32) {
+        switch (head_dim) {
+        case 64: return tma ? launch_decode_dt<64, true, 32>(p, tk, tv, num_items, s)
+                            : launch_decode_dt<64, false, 32>(p, tk, tv, num_items, s);
+        case 128: return tma ? launch_decode_dt<128, true, 32>(p, tk, tv, num_items, s)
+                             : launch_decode_dt<128, false, 32>(p, tk, tv, num_items, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (head_dim) {
-    case 64: return tma ? launch_decode_dt<64, true>(p, tk, tv, num_items, s)
-                        : launch_decode_dt<64, false>(p, tk, tv, num_items, s);
-    case 128: return tma ? launch_decode_dt<128, true>(p, tk, tv, num_items, s)
-                         : launch_decode_dt<128, false>(p, tk, tv, num_items, s);
-    case 256: return tma ? launch_decode_dt<256, true>(p, tk, tv, num_items, s)
-                         : launch_decode_dt<256, false>(p, tk, tv, num_items, s);
+    case 64: return tma ? launch_decode_dt<64, true, 64>(p, tk, tv, num_items, s)
+                        : launch_decode_dt<64, false, 64>(p, tk, tv, num_items, s);
+    case 128: return tma ? launch_decode_dt<128, true, 64>(p, tk, tv, num_items, s)
+                         : launch_decode_dt<128, false, 64>(p, tk, tv, num_items, s);
+    case 256: return tma ? launch_decode_dt<256, true, 64>(p, tk, tv, num_items, s)
+                         : launch_decode_dt<256, false, 64>(p, tk, tv, num_items, s);
     default: return cudaErrorInvalidValue;
     }
 }

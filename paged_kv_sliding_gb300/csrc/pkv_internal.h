@@ -57,7 +57,12 @@ struct DecodeItem {
     int32_t pbase;    // first partial slot of the request (split items)
     int32_t nsplit;   // splits of the request (split items)
     int32_t counter;  // arrival counter of this (request, KV head, head block) group
-    int32_t pad0, pad1;
+    // The request's facts the kernel needs, carried here so that a CTA's first
+    // page-table read does not wait behind a second dependent load.
+    int32_t row;            // the request's query row (its qo_begin)
+    int32_t kv_len;         // keys in the request's cache
+    int32_t kv_page_begin;  // the request's first entry in kv_indices
+    int32_t pad0;
 };
 
 // Merge of a request's split-KV partial states into its output row.
@@ -128,7 +133,10 @@ struct PrefillParams {
 };
 
 // Launchers (one per kernel family); return cudaGetLastError() of the launch.
-cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s);
+// tile: KV tokens per stage, 64 or (head_dim <= 128) 32.
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile);
+// KV tile of the decode kernel for a batch whose longest key range is max_keys.
+inline int decode_tile_for(int head_dim, int64_t max_keys) { return head_dim <= 128 && max_keys <= 192 ? 32 : 64; }
 // Page sizes whose pages the decode kernel loads with TMA boxes.
 bool decode_tma_page_size(int page_size);
 cudaError_t launch_merge_partials(const MergePartialsParams &p, int head_dim, cudaStream_t s);

@@ -154,8 +154,8 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
             for (int hk = 0; hk < d->num_kv_heads; ++hk)
                 for (int h0 = 0; h0 < group; h0 += kDecodeRows)
                     items.push_back({b, hk, hk * group + h0, std::min(kDecodeRows, group - h0), (int32_t)j0,
-                                     (int32_t)j1, n > 1 ? (int32_t)(pbase + s) : -1, pbase, (int32_t)n, -1, 0,
-                                     0});
+                                     (int32_t)j1, n > 1 ? (int32_t)(pbase + s) : -1, pbase, (int32_t)n, -1,
+                                     reqs[b].qo_begin, reqs[b].kv_len, reqs[b].kv_page_begin, 0});
         }
     }
     std::stable_sort(items.begin(), items.end(),
@@ -219,7 +219,10 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
     p.page_shift = page_shift(d->page_size);
     p.num_pages = d->num_pages;
     p.sm_scale_log2 = d->sm_scale * 1.4426950408889634f;
-    ce = launch_decode(p, d->head_dim, (int)items.size(), stream);
+    int64_t max_keys = 0;
+    for (const DecodeItem &it : items)
+        max_keys = std::max<int64_t>(max_keys, it.j1 - it.j0);
+    ce = launch_decode(p, d->head_dim, (int)items.size(), stream, decode_tile_for(d->head_dim, max_keys));
     if (ce != cudaSuccess)
         return noalloc_fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(ce));
     if (!merges.empty()) {
