@@ -420,7 +420,8 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
         std::stable_sort(d_items.begin(), d_items.end(), [](const DecodeItem &a, const DecodeItem &b) {
             return (a.j1 - a.j0) > (b.j1 - b.j0);
         });
-        decode_tile = decode_tile_for(d.head_dim, d_items.empty() ? 0 : d_items.front().j1 - d_items.front().j0);
+        decode_tile = decode_tile_for(d.head_dim, d_items.empty() ? 0 : d_items.front().j1 - d_items.front().j0,
+                                      (int64_t)d_items.size(), device_sm_count(device));
     }
 
     // One device workspace: requests | items | merge items | partial o | partial lse | status.

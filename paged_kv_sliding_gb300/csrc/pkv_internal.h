@@ -135,8 +135,20 @@ struct PrefillParams {
 // Launchers (one per kernel family); return cudaGetLastError() of the launch.
 // tile: KV tokens per stage, 64 or (head_dim <= 128) 32.
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile);
-// KV tile of the decode kernel for a batch whose longest key range is max_keys.
-inline int decode_tile_for(int head_dim, int64_t max_keys) { return head_dim <= 128 && max_keys <= 192 ? 32 : 64; }
+// KV tile of the decode kernel (head_dim <= 128): 32 tokens (4 CTAs per SM) for
+// short key ranges, which are latency-bound, and for medium ones (<= 1024 keys)
+// whose CTAs need more than one wave at 2 per SM but fit in one at 4; otherwise 64
+// (twice the bytes in flight per CTA, which long ranges need).
+inline int decode_tile_for(int head_dim, int64_t max_keys, int64_t n_items, int n_sm)
+{
+    if (head_dim > 128)
+        return 64;
+    if (max_keys <= 192)
+        return 32;
+    if (max_keys <= 1024 && n_items > 2LL * n_sm && n_items <= 4LL * n_sm)
+        return 32;
+    return 64;
+}
 // Page sizes whose pages the decode kernel loads with TMA boxes.
 bool decode_tma_page_size(int page_size);
 cudaError_t launch_merge_partials(const MergePartialsParams &p, int head_dim, cudaStream_t s);

@@ -222,7 +222,11 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
     int64_t max_keys = 0;
     for (const DecodeItem &it : items)
         max_keys = std::max<int64_t>(max_keys, it.j1 - it.j0);
-    ce = launch_decode(p, d->head_dim, (int)items.size(), stream, decode_tile_for(d->head_dim, max_keys));
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    ce = launch_decode(p, d->head_dim, (int)items.size(), stream,
+                       decode_tile_for(d->head_dim, max_keys, (int64_t)items.size(), sms));
     if (ce != cudaSuccess)
         return noalloc_fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(ce));
     if (!merges.empty()) {
