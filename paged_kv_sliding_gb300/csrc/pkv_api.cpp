@@ -316,25 +316,29 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     if (d.kind == PKV_PREFILL) {
         const int T = prefill_kv_tile(d.head_dim);
         const int tq = prefill_tokens_per_cta(d.head_dim, group);
+        const int64_t kv_align =
+            prefill_pp_tma_page_size(d.page_size, d.head_dim) ? std::min(d.page_size, T) : 1;
         for (int b = 0; b < B; ++b) {
             const HostRequest &r = reqs[b];
             for (int64_t t0 = 0; t0 < r.qo_len; t0 += tq) {
                 int64_t nt = std::min<int64_t>(tq, r.qo_len - t0);
                 int64_t lo, hi;
                 visible_interval(r.q_start + t0, r.q_start + t0 + nt - 1, r.kv_len, W, causal, lo, hi);
-                int32_t tlo = 0, thi = 0;
+                // The item's KV tiles start at its first visible key, rounded down
+                // only as far as the loader needs (a page for TMA page boxes), not
+                // to a multiple of the tile: the window then spans the fewest tiles.
+                int32_t start = 0, ntl = 0;
                 if (hi >= lo) {
-                    tlo = (int32_t)(lo / T);
-                    thi = (int32_t)(hi / T + 1);
+                    start = (int32_t)(lo / kv_align * kv_align);
+                    ntl = (int32_t)((hi - start) / T + 1);
                 }
                 // Start tile: the query block's index times the golden ratio,
                 // modulo the tile count, so that neighbouring blocks (which run at
                 // the same time over nearly the same KV tiles) start far apart.
-                const int32_t ntl = thi - tlo;
                 const double frac = std::fmod((double)(t0 / tq) * 0.6180339887498949, 1.0);
                 const int32_t rot = ntl > 1 ? std::min<int32_t>(ntl - 1, (int32_t)(frac * ntl)) : 0;
                 for (int hk = 0; hk < d.num_kv_heads; ++hk)
-                    p_items.push_back({b, hk, (int32_t)t0, (int32_t)nt, tlo, thi, rot, 0});
+                    p_items.push_back({b, hk, (int32_t)t0, (int32_t)nt, start, ntl, rot, 0});
             }
         }
         // Persistent CTAs, one per SM: longest-processing-time-first assignment of
@@ -345,7 +349,7 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
         const int tq_tile = std::max(1, kPrefillRows / group);
         auto cost = [&](const PrefillItem &it) {
             const int nq = (d.head_dim <= 128 && it.ntok > tq_tile) ? 2 : 1;
-            return (it.kv_tile_hi - it.kv_tile_lo) * (nq == 2 ? 1.0 : 0.65) + 1.5;
+            return it.kv_tiles * (nq == 2 ? 1.0 : 0.65) + 1.5;
         };
         std::stable_sort(p_items.begin(), p_items.end(),
                          [&](const PrefillItem &a, const PrefillItem &b) { return cost(a) > cost(b); });

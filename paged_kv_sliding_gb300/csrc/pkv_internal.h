@@ -21,28 +21,28 @@ struct RequestInfo {
     int32_t pad0, pad1, pad2;
 };
 
-// One CTA of the prefill kernel: a tile of packed query rows (query tokens x the
-// KV head's query-head group) of one request against the KV tiles
-// [kv_tile_lo, kv_tile_hi) that its positions can see.
+// One work item of the prefill kernel: one or two tiles of packed query rows (query
+// tokens x the KV head's query-head group) of one request against the kv_tiles KV
+// tiles from key kv_start on, which cover every key its positions can see.
 struct PrefillItem {
     int32_t req;
     int32_t kv_head;
     int32_t tok0;        // first query token of the tile, within the request
     int32_t ntok;        // query tokens in the tile
-    int32_t kv_tile_lo;  // first KV tile (in units of the kernel's KV tile)
-    int32_t kv_tile_hi;  // one past the last KV tile
-    int32_t kv_tile_rot; // tiles are visited from kv_tile_lo + kv_tile_rot, wrapping around
+    int32_t kv_start;    // first key of the item's first KV tile (aligned for the loader)
+    int32_t kv_tiles;    // KV tiles of the item (0: no visible key)
+    int32_t kv_tile_rot; // tiles are visited from tile kv_tile_rot on, wrapping around
     int32_t pad0;
 };
 
-// The KV tile visited at step j (0 <= j < hi - lo) of a prefill item. Softmax
-// accumulation is order-independent; staggering the start keeps the items that
-// run at the same time on one KV head from all missing L2 on the same tile.
-__host__ __device__ inline int prefill_kv_tile_at(const PrefillItem &it, int j)
+// First key of the KV tile visited at step j (0 <= j < kv_tiles) of a prefill item
+// whose tiles hold T keys. Softmax accumulation is order-independent; staggering the
+// start keeps the items that run at the same time on one KV head from all missing L2
+// on the same tile.
+__host__ __device__ inline int prefill_kv_key_at(const PrefillItem &it, int j, int T)
 {
-    const int n = it.kv_tile_hi - it.kv_tile_lo;
     const int k = j + it.kv_tile_rot;
-    return it.kv_tile_lo + (k < n ? k : k - n);
+    return it.kv_start + (k < it.kv_tiles ? k : k - it.kv_tiles) * T;
 }
 
 // One CTA of the decode kernel: up to kDecodeRows query heads of one request's

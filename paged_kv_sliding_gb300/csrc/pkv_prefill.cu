@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(384, 1)
             if (wg >= q_tiles(it))
                 continue;
             const RequestInfo rq = p.reqs[it.req];
-            const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
+            const int n_tiles = it.kv_tiles;
             const int ntok_wg = min(tq, it.ntok - wg * tq);
             const int tok = it.tok0 + wg * tq + r / g;
             const int pos = rq.q_start + tok;
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(384, 1)
                     tmem_ld32(tS + 32 * c, *reinterpret_cast<float(*)[32]>(&s[32 * c]));
                 tmem_wait_ld();
 
-                const int j0 = prefill_kv_tile_at(it, j) * T;
+                const int j0 = prefill_kv_key_at(it, j, T);
                 bool need_mask = j0 + T > rq.kv_len;
                 if (kCausal)
                     need_mask |= j0 + T - 1 > p_min;
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(384, 1)
             // The next item at or after ii that has KV tiles (items without any
             // only write zeros and take no part in the pipeline).
             auto next_busy = [&](int ii) {
-                while (ii < item_hi && p.items[ii].kv_tile_hi <= p.items[ii].kv_tile_lo)
+                while (ii < item_hi && p.items[ii].kv_tiles <= 0)
                     ++ii;
                 return ii;
             };
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(384, 1)
             while (ok && ii < item_hi) {
                 const PrefillItem it = p.items[ii];
                 const int nq = q_tiles(it);
-                const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
+                const int n_tiles = it.kv_tiles;
                 const int ii_next = next_busy(ii + 1);
                 if (!(ok = wait(B::kQ, n_q & 1)))
                     break;
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(384, 1)
             bool okp = true;
             for (int ii = item_lo; okp && ii < item_hi; ++ii) {
                 const PrefillItem it = p.items[ii];
-                const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
+                const int n_tiles = it.kv_tiles;
                 if (n_tiles <= 0)
                     continue;
                 const RequestInfo rq = p.reqs[it.req];
@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(384, 1)
                 auto load_id = [&](int j) -> int {
                     if (lane >= npg)
                         return -1;
-                    const int j0 = prefill_kv_tile_at(it, j) * T;
+                    const int j0 = prefill_kv_key_at(it, j, T);
                     const int lp = P <= T ? j0 / P + lane : j0 / P;
                     if (lp >= n_pages_req)
                         return -1;
@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(384, 1)
                 };
                 int pg = load_id(0);
                 for (int j = 0; okp && j < n_tiles; ++j) {
-                    const int j0 = prefill_kv_tile_at(it, j) * T;
+                    const int j0 = prefill_kv_key_at(it, j, T);
                     const int slot0 = P > T ? j0 % P : 0;
                     int pg_next = -1;
                     // K, then V. Both complete the K slot's barrier; a V tile reaching
@@ -575,13 +575,13 @@ __global__ void __launch_bounds__(384, 1)
                     c_page_begin = r.kv_page_begin;
                     c_at = c_ii;
                 }
-                if (c_j < c_it.kv_tile_hi - c_it.kv_tile_lo)
+                if (c_j < c_it.kv_tiles)
                     break;
                 ++c_ii;
                 c_j = 0;
             }
             if (c_ii < item_hi) {
-                const int j0 = prefill_kv_tile_at(c_it, c_j) * T;
+                const int j0 = prefill_kv_key_at(c_it, c_j, T);
                 for (int t = pt; t < T; t += NP) {
                     int *dst = &id_ring[(n_ids % kIdRing) * Tr::kIdsPerTile + t];
                     const int jj = j0 + t;
@@ -605,11 +605,11 @@ __global__ void __launch_bounds__(384, 1)
         bool okp = true;
         for (int ii = item_lo; okp && ii < item_hi; ++ii) {
             const PrefillItem it = p.items[ii];
-            const int n_tiles = it.kv_tile_hi - it.kv_tile_lo;
+            const int n_tiles = it.kv_tiles;
             if (n_tiles <= 0)
                 continue;
             for (int j = 0; okp && j < n_tiles; ++j, ++n_t) {
-                const int j0 = prefill_kv_tile_at(it, j) * T;
+                const int j0 = prefill_kv_key_at(it, j, T);
                 sync_producers();  // every producer is done with the ring entry refilled next
                 fetch_ids();
                 cp_async_wait<kIdRing - 1>();
