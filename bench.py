@@ -6,7 +6,7 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 One step = one pass of the whole hot path over the batch-decode workload: 64
 requests with kv_len ~ U[256, 4096], 32 query / 8 KV heads, head_dim 128, page 16,
 once for each window_left in {-1, 0, 31, 127, 1023} (plans made beforehand; each
-run = split-KV decode kernel + LSE merge kernel). The metric is the algorithmic KV
+run = one decode kernel, which also merges split-KV partials when a plan splits). The metric is the algorithmic KV
 bytes read (visible rows x 2 x H_kv x d x 2 B) per second. The line also carries
 the prefill (TFLOP/s) and long-context decode (GB/s) workloads under "workloads".
 
@@ -39,6 +39,21 @@ METRIC = "prefill TFLOP/s + decode KV GB/s, paged SWA attn, 1 GB300, % of roofli
 UNIT = "GB/s"
 WORKLOAD = ("batch decode: 64 requests, kv_len U[256,4096], 32q/8kv heads, d 128, page 16, "
             "window_left in {-1,0,31,127,1023}, bf16, lse")
+
+
+def _max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The largest of the ranks' values, returned on every rank (the slowest rank's
+    time is the job's time)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the job's time."""
+    return world * units_per_rank / seconds
 
 
 def _peaks():
@@ -316,14 +331,10 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = _max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     step_bytes = sum(bytes_per)
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = _job_rate(step_bytes, world, ms_per_step * 1e-3) / 1e9
 
     # dominant kernel: the decode kernel's window_left = -1 launch (the largest
     # share of the step), averaged over the timed steps
@@ -338,6 +349,7 @@ def run_ours(args, rank, world):
     traffic = _profiled_traffic("decode", "batch_decode", "pkv_decode.cu")
 
     e2e_s, h2d, d2h = e2e_decode(pkv, w, windows, max(3, args.steps // 4), 2)
+    e2e_s = _max_over_ranks(e2e_s, world)
     del plans, runs
     torch.cuda.empty_cache()
 
@@ -356,7 +368,7 @@ def run_ours(args, rank, world):
                      "traffic": traffic, "kernel": "pkv decode_kernel<128>, window_left -1 launch",
                      "algorithmic_bytes": bytes_per[i_full], "kernel_us": round(1e3 * kern_full, 2),
                      "peak_source": peaks["source"]},
-        "e2e": {"value": round(world * step_bytes / e2e_s / 1e9, 2), "unit": UNIT,
+        "e2e": {"value": round(_job_rate(step_bytes, world, e2e_s) / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
         "per_window": per_window,
