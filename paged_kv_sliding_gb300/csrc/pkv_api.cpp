@@ -343,13 +343,13 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
         }
         // Persistent CTAs, one per SM: longest-processing-time-first assignment of
         // the items to the least loaded CTA. Cost of an item in KV-tile steps: a
-        // single query tile runs its softmax-bound chain alone (about 0.65 of the
-        // two-tile ping-pong step), plus a fixed cost per item (pipeline fill and
-        // epilogue).
+        // single query tile runs its softmax-bound chain alone (about 0.8 of the
+        // two-tile ping-pong step, as measured through the schedule it yields),
+        // plus a fixed cost per item (pipeline fill and epilogue).
         const int tq_tile = std::max(1, kPrefillRows / group);
         auto cost = [&](const PrefillItem &it) {
             const int nq = (d.head_dim <= 128 && it.ntok > tq_tile) ? 2 : 1;
-            return it.kv_tiles * (nq == 2 ? 1.0 : 0.65) + 1.5;
+            return it.kv_tiles * (nq == 2 ? 1.0 : 0.8) + 1.5;
         };
         std::stable_sort(p_items.begin(), p_items.end(),
                          [&](const PrefillItem &a, const PrefillItem &b) { return cost(a) > cost(b); });
