@@ -526,6 +526,7 @@ int pkv_plan_get_info(const pkv_plan *plan, pkv_plan_info *info)
     info->workspace_bytes = (int64_t)plan->workspace_bytes;
     info->total_q = plan->total_q;
     info->kernels_per_run = plan->num_items > 0 ? 1 + (plan->num_merge_items > 0 ? 1 : 0) : 0;
+    info->kv_tile = plan->desc.kind == PKV_DECODE ? plan->decode_tile : prefill_kv_tile(plan->desc.head_dim);
     return PKV_OK;
 }
 

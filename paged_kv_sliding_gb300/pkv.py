@@ -75,7 +75,7 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64),
         ("total_q", ctypes.c_int64),
         ("kernels_per_run", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("kv_tile", ctypes.c_int32),
     ]
 
 
@@ -197,7 +197,7 @@ class Plan:
     def get_info(self) -> dict:
         info = PlanInfo()
         _check(self._lib.pkv_plan_get_info(self._handle, ctypes.byref(info)), "pkv_plan_get_info")
-        return {k: getattr(info, k) for k, _ in PlanInfo._fields_ if k != "reserved"}
+        return {k: getattr(info, k) for k, _ in PlanInfo._fields_}
 
     def run(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,

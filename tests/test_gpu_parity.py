@@ -235,6 +235,21 @@ def test_decode_many_short_items(pkv, oracle_lib, P, d):
     assert info["num_work_items"] == 4 * len(kv)
 
 
+@pytest.mark.parametrize("P", [8, 32, 64, 128])
+@pytest.mark.parametrize("W,tile", [(100, 32), (3000, 64)])
+def test_decode_tiles_and_page_sizes(pkv, oracle_lib, P, W, tile):
+    """Both decode tiles (32 tokens for short key ranges, 64 otherwise) with TMA page
+    boxes of pages smaller than, equal to and larger than the tile."""
+    rng = np.random.default_rng(P + W)
+    kv = rng.integers(1, 3500, size=24).tolist()
+    w = wl.make_workload(name="tiles", kind="decode", qo_lens=np.ones(len(kv)), kv_lens=kv,
+                         num_qo_heads=16, num_kv_heads=4, head_dim=128, page_size=P, window_left=W,
+                         causal=True, seed=P * 3 + W, layout_rng=rng)
+    # unsplit, so that the long ranges stay long (split pieces would go to the 32-token tile)
+    _, info = check(pkv, oracle_lib, w, disable_split_kv=(tile == 64))
+    assert info["kv_tile"] == tile, info
+
+
 def test_decode_q_start_non_causal(pkv, oracle_lib):
     w = wl.make_workload(name="decq", kind="decode", qo_lens=np.ones(3), kv_lens=[100, 50, 10],
                          num_qo_heads=4, num_kv_heads=1, head_dim=64, page_size=8, window_left=7,
