@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define PKV_API __attribute__((visibility("default")))
@@ -143,6 +143,51 @@ typedef struct pkv_plan_info {
  * Returns PKV_OK and sets *out, or an error with *out = NULL.
  */
 PKV_API int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream);
+
+/* Capacity of a capturable plan. */
+typedef struct pkv_plan_caps {
+    int32_t max_batch;    /* requests any later batch may hold (>= 1) */
+    int32_t reserved;
+    int64_t max_total_q;  /* PREFILL: query rows any later batch may hold (>= 1); q, out
+                             and lse passed to pkv_run must hold this many rows. Ignored
+                             for DECODE (one row per request). */
+} pkv_plan_caps;
+
+/*
+ * pkv_plan_create_capturable: a plan whose pkv_run may be captured into a CUDA graph
+ * once and replayed for later batches re-planned with pkv_plan_update. The launch
+ * shapes are fixed by the capacity, not by the batch: the decode grid holds
+ * max_batch x H_kv x ceil(group/16) x 4 CTAs (at most 4 KV splits per request) and
+ * CTAs beyond the live work items return at once; prefill runs one persistent CTA per
+ * SM whose work lists may be empty. The kernel variant (mask mode, decode KV tile,
+ * TMA or cp.async gather) is chosen from this first batch and kept. This addresses
+ * the baked-grid failure of a captured paged-attention launch described on the
+ * AMD flashinfer PR #234 page ("Why each fix"), and the sync-free re-plan from host
+ * metadata of flashinfer_backend.py's fast_prefill_plan.
+ * Allocates the workspace for the capacity and two pinned staging images; the first
+ * upload is waited for, as in pkv_plan_create. Returns PKV_OK and sets *out, or
+ * PKV_ERR_INVALID_ARG (caps NULL, capacity below the batch) / the errors of
+ * pkv_plan_create, with *out = NULL.
+ */
+PKV_API int pkv_plan_create_capturable(pkv_plan **out, const pkv_plan_desc *desc, const pkv_plan_caps *caps,
+                                       void *stream);
+
+/*
+ * pkv_plan_update: re-plan a capturable plan for a new batch, in place: host arrays
+ * in `desc` (qo_indptr, kv_indptr, kv_last_page_len, q_start, batch_size,
+ * fixed_split_size, disable_split_kv) may change; kind, head counts, head_dim,
+ * page_size, window_left, causal, sm_scale, dtype, num_pages and the kv_indices
+ * device pointer must equal the plan's (the caller rewrites that array's contents,
+ * stream-ordered before the next run), else PKV_ERR_INVALID_ARG. A batch above the
+ * capacity returns PKV_ERR_UNSUPPORTED and leaves the plan unchanged.
+ * Allocates nothing and does not synchronise the device: the new schedule is written
+ * to a pinned staging image and copied into the workspace with cudaMemcpyAsync on
+ * `stream`, so runs issued later on that stream (or replays of a graph captured from
+ * pkv_run) see it, and runs issued earlier see the old one. The host waits only if
+ * the upload of two updates ago is still in flight. Must not be called while
+ * `stream` is being captured.
+ */
+PKV_API int pkv_plan_update(pkv_plan *plan, const pkv_plan_desc *desc, void *stream);
 
 /*
  * pkv_run: attention for the planned batch. q, caches and out are DEVICE bf16

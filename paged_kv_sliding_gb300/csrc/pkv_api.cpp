@@ -55,8 +55,17 @@ struct pkv_plan {
     int mask_mode = kMaskNone;
     int num_items = 0;
     int num_partials = 0;
-    int num_merge_items = 0;
-    int num_ctas = 0;  // prefill: persistent CTAs
+    int num_ctas = 0;  // prefill: persistent CTAs (lists)
+    int n_sm = 0;
+    // Capturable plans: launch shapes and workspace sized by the declared capacity,
+    // re-planned in place by pkv_plan_update through two pinned staging images.
+    bool capturable = false;
+    int64_t cap_items = 0, cap_total_q = 0, cap_batch = 0;
+    size_t upload_bytes = 0;
+    void *staging[2] = {nullptr, nullptr};
+    cudaEvent_t staging_done[2] = {nullptr, nullptr};
+    int staging_next = 0;
+    int32_t *d_live = nullptr;  // live work items (capturable decode launches exit above it)
     int decode_tile = 64;  // decode: KV tokens per stage of the kernel
     int64_t total_q = 0;
     const int32_t *kv_indices = nullptr;  // borrowed device pointer
@@ -64,7 +73,6 @@ struct pkv_plan {
     size_t workspace_bytes = 0;
     RequestInfo *d_reqs = nullptr;
     void *d_items = nullptr;
-    MergeItem *d_merge = nullptr;
     int32_t *d_cta_items = nullptr;
     float *d_partial_o = nullptr;
     float *d_partial_lse = nullptr;
@@ -252,49 +260,35 @@ int64_t choose_decode_chunk(const std::vector<int64_t> &lens, int head_blocks, i
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-const char *pkv_status_string(int status)
+// The work schedule of a batch, built on the host from the host arrays alone.
+struct Schedule {
+    std::vector<RequestInfo> reqs;
+    std::vector<PrefillItem> p_items;
+    std::vector<DecodeItem> d_items;
+    std::vector<int32_t> cta_items;  // prefill: list offsets (lists + 1 entries)
+    int num_partials = 0;
+    int num_counters = 0;
+    int mask_mode = kMaskNone;
+    int decode_tile = 64;
+    int64_t total_q = 0;
+};
+
+// Splits per request that a capturable decode plan's workspace holds.
+constexpr int kCapturableMaxSplits = 4;
+
+// capturable: one prefill list per SM and at most kCapturableMaxSplits decode splits
+// per request; fixed_tile > 0: the decode tile to use (a captured launch's variant).
+void build_schedule(const pkv_plan_desc &d, const std::vector<HostRequest> &reqs, int device, bool capturable,
+                    int fixed_tile, Schedule &sc)
 {
-    switch (status) {
-    case PKV_OK: return "PKV_OK";
-    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
-    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
-    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
-    case PKV_ERR_OOM: return "PKV_ERR_OOM";
-    case PKV_ERR_DEVICE_BOUNDS: return "PKV_ERR_DEVICE_BOUNDS";
-    case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
-    default: return "PKV_ERR_UNKNOWN";
-    }
-}
-
-const char *pkv_last_error(void) { return g_last_error.c_str(); }
-
-int pkv_abi_version(void) { return PKV_ABI_VERSION; }
-
-int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
-{
-    g_last_error.clear();
-    if (!out)
-        return fail(PKV_ERR_INVALID_ARG, "out is NULL");
-    *out = nullptr;
-    std::vector<HostRequest> reqs;
-    int st = validate(desc, reqs);
-    if (st != PKV_OK)
-        return st;
-    const pkv_plan_desc &d = *desc;
-    cudaStream_t stream = (cudaStream_t)stream_;
     const int B = d.batch_size;
     const int group = d.num_qo_heads / d.num_kv_heads;
     const bool causal = d.causal != 0;
     const int W = d.window_left < 0 ? -1 : d.window_left;
-
-    int device = 0;
-    cudaError_t ce = cudaGetDevice(&device);
-    if (ce != cudaSuccess)
-        return cuda_fail(ce, "cudaGetDevice");
-
-    std::vector<RequestInfo> h_reqs(B);
+    std::vector<RequestInfo> &h_reqs = sc.reqs;
+    h_reqs.assign(B, RequestInfo{});
     int64_t total_q = 0;
     for (int b = 0; b < B; ++b) {
         const HostRequest &r = reqs[b];
@@ -303,10 +297,9 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
         total_q = std::max<int64_t>(total_q, r.qo_begin + r.qo_len);
     }
 
-    std::vector<PrefillItem> p_items;
-    std::vector<DecodeItem> d_items;
-    std::vector<MergeItem> m_items;
-    std::vector<int32_t> cta_items;  // prefill: per-CTA item offsets
+    std::vector<PrefillItem> &p_items = sc.p_items;
+    std::vector<DecodeItem> &d_items = sc.d_items;
+    std::vector<int32_t> &cta_items = sc.cta_items;  // prefill: per-list item offsets
     int decode_tile = 64;
     int num_partials = 0;
     int num_counters = 0;
@@ -354,7 +347,9 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
         std::stable_sort(p_items.begin(), p_items.end(),
                          [&](const PrefillItem &a, const PrefillItem &b) { return cost(a) > cost(b); });
         const int n_sm = device_sm_count(device);
-        const int G = (int)std::min<size_t>(p_items.size(), (size_t)n_sm);
+        // A capturable plan keeps one list per SM (some may be empty): the launch's
+        // grid is fixed when it is captured.
+        const int G = capturable ? n_sm : (int)std::min<size_t>(p_items.size(), (size_t)n_sm);
         std::vector<std::vector<PrefillItem>> per_cta(G);
         std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>,
                             std::greater<std::pair<double, int>>>
@@ -402,6 +397,12 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
                                 : 0;
             if (L > 0)
                 n = (L + per - 1) / per;
+            if (capturable && n > kCapturableMaxSplits) {
+                // the workspace of a capturable plan holds this many splits per request
+                n = kCapturableMaxSplits;
+                per = round_up((L + n - 1) / n, 16);
+                n = (L + per - 1) / per;
+            }
             int32_t pbase = -1, cbase = -1;
             if (n > 1) {
                 pbase = num_partials;
@@ -424,12 +425,65 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
         std::stable_sort(d_items.begin(), d_items.end(), [](const DecodeItem &a, const DecodeItem &b) {
             return (a.j1 - a.j0) > (b.j1 - b.j0);
         });
-        decode_tile = decode_tile_for(d.head_dim, d_items.empty() ? 0 : d_items.front().j1 - d_items.front().j0,
-                                      (int64_t)d_items.size(), device_sm_count(device));
+        decode_tile = fixed_tile > 0 ? fixed_tile
+                                     : decode_tile_for(d.head_dim,
+                                                       d_items.empty() ? 0 : d_items.front().j1 - d_items.front().j0,
+                                                       (int64_t)d_items.size(), device_sm_count(device));
     }
+    sc.num_partials = num_partials;
+    sc.num_counters = num_counters;
+    sc.mask_mode = mask_mode;
+    sc.decode_tile = decode_tile;
+    sc.total_q = total_q;
 
-    // One device workspace: requests | items | merge items | partial o | partial lse | status.
-    const size_t n_items = d.kind == PKV_PREFILL ? p_items.size() : d_items.size();
+}
+
+// Sizes of a plan's device workspace: the live schedule for an ordinary plan, the
+// declared capacity for a capturable one.
+struct Caps {
+    int64_t batch = 0, total_q = 0, items = 0, lists = 0, partials = 0, counters = 0;
+};
+
+Caps caps_of(const pkv_plan_desc &d, const Schedule &sc)
+{
+    Caps c;
+    c.batch = d.batch_size;
+    c.total_q = sc.total_q;
+    c.items = d.kind == PKV_PREFILL ? (int64_t)sc.p_items.size() : (int64_t)sc.d_items.size();
+    c.lists = sc.cta_items.empty() ? 0 : (int64_t)sc.cta_items.size() - 1;
+    c.partials = sc.num_partials;
+    c.counters = sc.num_counters;
+    return c;
+}
+
+Caps caps_for_capacity(const pkv_plan_desc &d, const pkv_plan_caps &cap, int n_sm)
+{
+    const int group = d.num_qo_heads / d.num_kv_heads;
+    Caps c;
+    c.batch = cap.max_batch;
+    if (d.kind == PKV_PREFILL) {
+        const int64_t tq = prefill_tokens_per_cta(d.head_dim, group);
+        c.total_q = cap.max_total_q;
+        c.items = (int64_t)d.num_kv_heads * ((cap.max_total_q + tq - 1) / tq + cap.max_batch);
+        c.lists = n_sm;
+    } else {
+        const int64_t head_blocks = (group + kDecodeRows - 1) / kDecodeRows;
+        c.total_q = cap.max_batch;
+        c.items = (int64_t)cap.max_batch * d.num_kv_heads * head_blocks * kCapturableMaxSplits;
+        c.partials = (int64_t)cap.max_batch * kCapturableMaxSplits;
+        c.counters = (int64_t)cap.max_batch * d.num_kv_heads * head_blocks;
+    }
+    return c;
+}
+
+// requests | items | list offsets | live item count (uploaded) | partial o | partial
+// lse | arrival counters | status.
+struct Layout {
+    size_t reqs, items, cta, live, po, pl, cnt, status, bytes, upload;
+};
+
+Layout layout_for(const pkv_plan_desc &d, const Caps &c)
+{
     const size_t item_bytes = d.kind == PKV_PREFILL ? sizeof(PrefillItem) : sizeof(DecodeItem);
     size_t off = 0;
     auto carve = [&](size_t bytes) {
@@ -437,42 +491,121 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
         off = (size_t)round_up((int64_t)(off + bytes), 256);
         return at;
     };
-    const size_t o_reqs = carve(sizeof(RequestInfo) * std::max<size_t>(1, B));
-    const size_t o_items = carve(item_bytes * std::max<size_t>(1, n_items));
-    const size_t o_merge = carve(sizeof(MergeItem) * std::max<size_t>(1, m_items.size()));
-    const size_t o_cta = carve(sizeof(int32_t) * std::max<size_t>(1, cta_items.size()));
-    const size_t o_po = carve(sizeof(float) * (size_t)num_partials * d.num_qo_heads * d.head_dim);
-    const size_t o_pl = carve(sizeof(float) * (size_t)num_partials * d.num_qo_heads);
-    const size_t o_cnt = carve(sizeof(int32_t) * std::max(1, num_counters));
-    const size_t o_status = carve(sizeof(int32_t) * 4);
-    const size_t ws_bytes = off;
-    const size_t upload_bytes = o_po;  // requests, items and merge items are uploaded
+    Layout l{};
+    l.reqs = carve(sizeof(RequestInfo) * std::max<int64_t>(1, c.batch));
+    l.items = carve(item_bytes * std::max<int64_t>(1, c.items));
+    l.cta = carve(sizeof(int32_t) * (std::max<int64_t>(0, c.lists) + 1));
+    l.live = carve(sizeof(int32_t) * 4);
+    l.po = carve(sizeof(float) * (size_t)c.partials * d.num_qo_heads * d.head_dim);
+    l.pl = carve(sizeof(float) * (size_t)c.partials * d.num_qo_heads);
+    l.cnt = carve(sizeof(int32_t) * std::max<int64_t>(1, c.counters));
+    l.status = carve(sizeof(int32_t) * 4);
+    l.bytes = off;
+    l.upload = l.po;
+    return l;
+}
+
+// The uploaded part of the workspace image of a schedule.
+void fill_image(const pkv_plan_desc &d, const Schedule &sc, const Layout &l, uint8_t *img)
+{
+    std::memset(img, 0, l.upload);
+    std::memcpy(img + l.reqs, sc.reqs.data(), sizeof(RequestInfo) * sc.reqs.size());
+    if (d.kind == PKV_PREFILL)
+        std::memcpy(img + l.items, sc.p_items.data(), sizeof(PrefillItem) * sc.p_items.size());
+    else
+        std::memcpy(img + l.items, sc.d_items.data(), sizeof(DecodeItem) * sc.d_items.size());
+    std::memcpy(img + l.cta, sc.cta_items.data(), sizeof(int32_t) * sc.cta_items.size());
+    const int32_t live = d.kind == PKV_PREFILL ? (int32_t)sc.p_items.size() : (int32_t)sc.d_items.size();
+    std::memcpy(img + l.live, &live, sizeof(live));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_status_string(int status)
+{
+    switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_OOM: return "PKV_ERR_OOM";
+    case PKV_ERR_DEVICE_BOUNDS: return "PKV_ERR_DEVICE_BOUNDS";
+    case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+    default: return "PKV_ERR_UNKNOWN";
+    }
+}
+
+const char *pkv_last_error(void) { return g_last_error.c_str(); }
+
+int pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+namespace {
+
+int create_plan(pkv_plan **out, const pkv_plan_desc *desc, const pkv_plan_caps *capacity, void *stream_)
+{
+    g_last_error.clear();
+    if (!out)
+        return fail(PKV_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    std::vector<HostRequest> reqs;
+    int st = validate(desc, reqs);
+    if (st != PKV_OK)
+        return st;
+    const pkv_plan_desc &d = *desc;
+    const bool capturable = capacity != nullptr;
+    if (capturable && (capacity->max_batch < d.batch_size || capacity->max_batch < 1 ||
+                       (d.kind == PKV_PREFILL && capacity->max_total_q < 1)))
+        return fail(PKV_ERR_INVALID_ARG, "capacity: max_batch must be >= 1 and >= batch_size%s",
+                    d.kind == PKV_PREFILL ? ", max_total_q >= 1" : "");
+    cudaStream_t stream = (cudaStream_t)stream_;
+    int device = 0;
+    cudaError_t ce = cudaGetDevice(&device);
+    if (ce != cudaSuccess)
+        return cuda_fail(ce, "cudaGetDevice");
+    const int n_sm = device_sm_count(device);
+
+    Schedule sc;
+    build_schedule(d, reqs, device, capturable, 0, sc);
+    const Caps caps = capturable ? caps_for_capacity(d, *capacity, n_sm) : caps_of(d, sc);
+    if (capturable && (sc.total_q > caps.total_q))
+        return fail(PKV_ERR_UNSUPPORTED, "the batch has %lld query rows, the capacity %lld",
+                    (long long)sc.total_q, (long long)caps.total_q);
+    const Layout lay = layout_for(d, caps);
 
     pkv_plan *plan = new (std::nothrow) pkv_plan();
     if (!plan)
         return fail(PKV_ERR_OOM, "host allocation of the plan failed");
-    ce = cudaMalloc(&plan->workspace, ws_bytes);
+    ce = cudaMalloc(&plan->workspace, lay.bytes);
     if (ce != cudaSuccess) {
         delete plan;
         return cuda_fail(ce, "cudaMalloc(plan workspace)");
     }
-    std::vector<uint8_t> staging(upload_bytes, 0);
-    std::memcpy(staging.data() + o_reqs, h_reqs.data(), sizeof(RequestInfo) * B);
-    if (d.kind == PKV_PREFILL)
-        std::memcpy(staging.data() + o_items, p_items.data(), item_bytes * n_items);
-    else
-        std::memcpy(staging.data() + o_items, d_items.data(), item_bytes * n_items);
-    std::memcpy(staging.data() + o_merge, m_items.data(), sizeof(MergeItem) * m_items.size());
-    std::memcpy(staging.data() + o_cta, cta_items.data(), sizeof(int32_t) * cta_items.size());
+    std::vector<uint8_t> image(lay.upload, 0);
+    fill_image(d, sc, lay, image.data());
     uint8_t *base = (uint8_t *)plan->workspace;
-    ce = cudaMemcpyAsync(base, staging.data(), upload_bytes, cudaMemcpyHostToDevice, stream);
+    ce = cudaMemcpyAsync(base, image.data(), lay.upload, cudaMemcpyHostToDevice, stream);
     if (ce == cudaSuccess)
-        ce = cudaMemsetAsync(base + o_status, 0, sizeof(int32_t) * 4, stream);
+        ce = cudaMemsetAsync(base + lay.status, 0, sizeof(int32_t) * 4, stream);
     if (ce == cudaSuccess)  // arrival counters start at zero; each merge resets its own
-        ce = cudaMemsetAsync(base + o_cnt, 0, sizeof(int32_t) * std::max(1, num_counters), stream);
+        ce = cudaMemsetAsync(base + lay.cnt, 0, lay.status - lay.cnt, stream);
     if (ce == cudaSuccess)
-        ce = cudaStreamSynchronize(stream);  // the staging buffer is freed on return
+        ce = cudaStreamSynchronize(stream);  // the host image is freed on return
+    if (ce == cudaSuccess && capturable) {
+        for (int k = 0; k < 2 && ce == cudaSuccess; ++k) {
+            ce = cudaHostAlloc(&plan->staging[k], lay.upload, cudaHostAllocDefault);
+            if (ce == cudaSuccess)
+                ce = cudaEventCreateWithFlags(&plan->staging_done[k], cudaEventDisableTiming);
+        }
+    }
     if (ce != cudaSuccess) {
+        for (int k = 0; k < 2; ++k) {
+            if (plan->staging[k])
+                cudaFreeHost(plan->staging[k]);
+            if (plan->staging_done[k])
+                cudaEventDestroy(plan->staging_done[k]);
+        }
         cudaFree(plan->workspace);
         delete plan;
         return cuda_fail(ce, "uploading the plan");
@@ -480,26 +613,112 @@ int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream_)
     plan->desc = d;
     plan->desc.qo_indptr = plan->desc.kv_indptr = plan->desc.kv_last_page_len = nullptr;
     plan->desc.q_start = nullptr;
-    plan->desc.window_left = W;
+    plan->desc.window_left = d.window_left < 0 ? -1 : d.window_left;
     plan->device = device;
-    plan->mask_mode = mask_mode;
-    plan->num_items = (int)n_items;
-    plan->num_partials = num_partials;
-    plan->num_merge_items = (int)m_items.size();
-    plan->num_ctas = cta_items.empty() ? 0 : (int)cta_items.size() - 1;
-    plan->decode_tile = decode_tile;
-    plan->total_q = total_q;
+    plan->n_sm = n_sm;
+    plan->capturable = capturable;
+    plan->mask_mode = sc.mask_mode;
+    plan->num_items = (int)(d.kind == PKV_PREFILL ? sc.p_items.size() : sc.d_items.size());
+    plan->num_partials = sc.num_partials;
+    plan->num_ctas = sc.cta_items.empty() ? 0 : (int)sc.cta_items.size() - 1;
+    plan->decode_tile = sc.decode_tile;
+    plan->total_q = sc.total_q;
+    plan->cap_items = caps.items;
+    plan->cap_total_q = caps.total_q;
+    plan->cap_batch = caps.batch;
+    plan->upload_bytes = lay.upload;
     plan->kv_indices = d.kv_indices;
-    plan->workspace_bytes = ws_bytes;
-    plan->d_reqs = (RequestInfo *)(base + o_reqs);
-    plan->d_items = base + o_items;
-    plan->d_merge = (MergeItem *)(base + o_merge);
-    plan->d_cta_items = (int32_t *)(base + o_cta);
-    plan->d_partial_o = (float *)(base + o_po);
-    plan->d_partial_lse = (float *)(base + o_pl);
-    plan->d_status = (int32_t *)(base + o_status);
-    plan->d_counters = (int32_t *)(base + o_cnt);
+    plan->workspace_bytes = lay.bytes;
+    plan->d_reqs = (RequestInfo *)(base + lay.reqs);
+    plan->d_items = base + lay.items;
+    plan->d_cta_items = (int32_t *)(base + lay.cta);
+    plan->d_live = (int32_t *)(base + lay.live);
+    plan->d_partial_o = (float *)(base + lay.po);
+    plan->d_partial_lse = (float *)(base + lay.pl);
+    plan->d_status = (int32_t *)(base + lay.status);
+    plan->d_counters = (int32_t *)(base + lay.cnt);
     *out = plan;
+    return PKV_OK;
+}
+
+}  // namespace
+
+int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream)
+{
+    return create_plan(out, desc, nullptr, stream);
+}
+
+int pkv_plan_create_capturable(pkv_plan **out, const pkv_plan_desc *desc, const pkv_plan_caps *caps,
+                               void *stream)
+{
+    if (!caps) {
+        g_last_error.clear();
+        if (out)
+            *out = nullptr;
+        return fail(PKV_ERR_INVALID_ARG, "caps is NULL");
+    }
+    return create_plan(out, desc, caps, stream);
+}
+
+int pkv_plan_update(pkv_plan *plan, const pkv_plan_desc *desc, void *stream_)
+{
+    g_last_error.clear();
+    if (!plan)
+        return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->capturable)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_plan_update needs a plan from pkv_plan_create_capturable");
+    std::vector<HostRequest> reqs;
+    int st = validate(desc, reqs);
+    if (st != PKV_OK)
+        return st;
+    const pkv_plan_desc &d = *desc, &o = plan->desc;
+    const int W = d.window_left < 0 ? -1 : d.window_left;
+    // What the captured launches bake in must not change.
+    if (d.kind != o.kind || d.num_qo_heads != o.num_qo_heads || d.num_kv_heads != o.num_kv_heads ||
+        d.head_dim != o.head_dim || d.page_size != o.page_size || W != o.window_left ||
+        (d.causal != 0) != (o.causal != 0) || d.sm_scale != o.sm_scale || d.dtype != o.dtype ||
+        d.num_pages != o.num_pages || d.kv_indices != o.kv_indices)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "update must keep kind, heads, head_dim, page_size, window_left, causal, sm_scale, "
+                    "dtype, num_pages and the kv_indices pointer of the plan");
+    if (d.batch_size > plan->cap_batch)
+        return fail(PKV_ERR_UNSUPPORTED, "batch %d exceeds the plan's capacity %lld", d.batch_size,
+                    (long long)plan->cap_batch);
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device)
+        return fail(PKV_ERR_INVALID_ARG, "plan was made on device %d, current device is %d", plan->device, cur);
+    Schedule sc;
+    build_schedule(d, reqs, plan->device, true, plan->decode_tile, sc);
+    const int64_t items = d.kind == PKV_PREFILL ? (int64_t)sc.p_items.size() : (int64_t)sc.d_items.size();
+    if (sc.total_q > plan->cap_total_q || items > plan->cap_items)
+        return fail(PKV_ERR_UNSUPPORTED, "the batch needs %lld query rows and %lld work items, the capacity is %lld "
+                    "and %lld", (long long)sc.total_q, (long long)items, (long long)plan->cap_total_q,
+                    (long long)plan->cap_items);
+    pkv_plan_caps cap{};
+    cap.max_batch = (int32_t)plan->cap_batch;
+    cap.max_total_q = plan->cap_total_q;
+    const Layout lay = layout_for(plan->desc, caps_for_capacity(plan->desc, cap, plan->n_sm));
+    cudaStream_t stream = (cudaStream_t)stream_;
+    // Two pinned staging images, each reused only once its previous upload is done
+    // (an event wait that is normally already satisfied; nothing else waits).
+    const int k = plan->staging_next;
+    cudaError_t ce = cudaEventSynchronize(plan->staging_done[k]);
+    if (ce != cudaSuccess)
+        return cuda_fail(ce, "waiting for the staging image");
+    fill_image(plan->desc, sc, lay, (uint8_t *)plan->staging[k]);
+    ce = cudaMemcpyAsync(plan->workspace, plan->staging[k], lay.upload, cudaMemcpyHostToDevice, stream);
+    if (ce == cudaSuccess)
+        ce = cudaEventRecord(plan->staging_done[k], stream);
+    if (ce != cudaSuccess)
+        return cuda_fail(ce, "uploading the updated plan");
+    plan->staging_next = k ^ 1;
+    plan->num_items = (int)items;
+    plan->num_partials = sc.num_partials;
+    plan->num_ctas = sc.cta_items.empty() ? 0 : (int)sc.cta_items.size() - 1;
+    plan->total_q = sc.total_q;
+    plan->desc.batch_size = d.batch_size;
+    plan->desc.fixed_split_size = d.fixed_split_size;
+    plan->desc.disable_split_kv = d.disable_split_kv;
     return PKV_OK;
 }
 
@@ -507,6 +726,14 @@ int pkv_plan_destroy(pkv_plan *plan)
 {
     if (!plan)
         return PKV_OK;
+    for (int k = 0; k < 2; ++k) {
+        if (plan->staging_done[k]) {
+            cudaEventSynchronize(plan->staging_done[k]);
+            cudaEventDestroy(plan->staging_done[k]);
+        }
+        if (plan->staging[k])
+            cudaFreeHost(plan->staging[k]);
+    }
     cudaError_t ce = cudaFree(plan->workspace);
     delete plan;
     if (ce != cudaSuccess)
@@ -525,7 +752,7 @@ int pkv_plan_get_info(const pkv_plan *plan, pkv_plan_info *info)
     info->mask_mode = plan->mask_mode;
     info->workspace_bytes = (int64_t)plan->workspace_bytes;
     info->total_q = plan->total_q;
-    info->kernels_per_run = plan->num_items > 0 ? 1 + (plan->num_merge_items > 0 ? 1 : 0) : 0;
+    info->kernels_per_run = (plan->num_items > 0 || plan->capturable) ? 1 : 0;
     info->kv_tile = plan->desc.kind == PKV_DECODE ? plan->decode_tile : prefill_kv_tile(plan->desc.head_dim);
     return PKV_OK;
 }
@@ -573,9 +800,9 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     g_last_error.clear();
     if (!plan)
         return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
-    if (plan->total_q > 0 && (!q || !out))
+    if ((plan->total_q > 0 || plan->capturable) && (!q || !out))
         return fail(PKV_ERR_INVALID_ARG, "q and out are required");
-    if (plan->num_items > 0 && (!k_cache || !v_cache))
+    if ((plan->num_items > 0 || plan->capturable) && (!k_cache || !v_cache))
         return fail(PKV_ERR_INVALID_ARG, "k_cache and v_cache are required");
     if (misaligned(q, 16) || misaligned(k_cache, 16) || misaligned(v_cache, 16) ||
         misaligned(out, 16) || misaligned(lse, 4))
@@ -584,7 +811,10 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     if (cudaGetDevice(&cur) == cudaSuccess && cur != plan->device)
         return fail(PKV_ERR_INVALID_ARG, "plan was made on device %d, current device is %d",
                     plan->device, cur);
-    if (plan->num_items == 0)
+    // A capturable plan always launches (its launch may be captured and replayed
+    // after pkv_plan_update); its decode grid is the capacity, its prefill grid one
+    // CTA per SM, and CTAs without work leave at once.
+    if (plan->num_items == 0 && !plan->capturable)
         return PKV_OK;
     cudaStream_t stream = (cudaStream_t)stream_;
     const pkv_plan_desc &d = plan->desc;
@@ -602,6 +832,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
         p.partial_o = plan->d_partial_o;
         p.partial_lse = plan->d_partial_lse;
         p.merge_counters = plan->d_counters;
+        p.live_items = plan->capturable ? plan->d_live : nullptr;
         p.status = plan->d_status;
         p.num_qo_heads = d.num_qo_heads;
         p.num_kv_heads = d.num_kv_heads;
@@ -611,24 +842,12 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
         p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
         if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
             return cuda_fail(ce, "cudaEventRecord");
-        ce = launch_decode(p, d.head_dim, plan->num_items, stream, plan->decode_tile);
+        ce = launch_decode(p, d.head_dim, plan->capturable ? (int)plan->cap_items : plan->num_items, stream,
+                           plan->decode_tile);
         if (ce != cudaSuccess)
             return cuda_fail(ce, "decode kernel launch");
         if (plan->ev_end && (ce = cudaEventRecord(plan->ev_end, stream)) != cudaSuccess)
             return cuda_fail(ce, "cudaEventRecord");
-        if (plan->num_merge_items > 0) {
-            MergePartialsParams m{};
-            m.items = plan->d_merge;
-            m.partial_o = plan->d_partial_o;
-            m.partial_lse = plan->d_partial_lse;
-            m.out = (uint16_t *)out;
-            m.lse = lse;
-            m.num_items = plan->num_merge_items;
-            m.num_qo_heads = d.num_qo_heads;
-            ce = launch_merge_partials(m, d.head_dim, stream);
-            if (ce != cudaSuccess)
-                return cuda_fail(ce, "split-KV merge launch");
-        }
         return PKV_OK;
     }
     PrefillParams p{};
@@ -646,7 +865,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.num_kv_heads = d.num_kv_heads;
     p.group = d.num_qo_heads / d.num_kv_heads;
     p.tokens_per_tile = std::max(1, kPrefillRows / p.group);
-    p.total_q = (int32_t)plan->total_q;
+    p.total_q = (int32_t)(plan->capturable ? plan->cap_total_q : plan->total_q);
     p.page_size = d.page_size;
     p.page_shift = page_shift_of(d.page_size);
     p.num_pages = d.num_pages;
@@ -654,7 +873,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
     if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
         return cuda_fail(ce, "cudaEventRecord");
-    ce = launch_prefill_pp(p, d.head_dim, plan->mask_mode, plan->num_ctas, stream);
+    ce = launch_prefill_pp(p, d.head_dim, plan->mask_mode, plan->capturable ? plan->n_sm : plan->num_ctas, stream);
     if (ce != cudaSuccess)
         return cuda_fail(ce, "prefill kernel launch");
     if (plan->ev_end && (ce = cudaEventRecord(plan->ev_end, stream)) != cudaSuccess)

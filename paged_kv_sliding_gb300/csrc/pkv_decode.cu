@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(DecTraits<D, TT>::kThreads, DecTraits<D, TT>::
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    if (p.live_items && (int)blockIdx.x >= *p.live_items)
+        return;  // a capturable plan's fixed grid: this CTA has no work item now
     const DecodeItem it = p.items[blockIdx.x];
     struct {
         int32_t qo_begin, kv_len, kv_page_begin;

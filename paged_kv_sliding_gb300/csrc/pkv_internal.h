@@ -80,6 +80,7 @@ enum MaskMode : int32_t { kMaskNone = 0, kMaskCausal = 1, kMaskCausalWindow = 2,
 
 struct DecodeParams {
     const DecodeItem *items;
+    const int32_t *live_items;  // non-NULL: CTAs at or above *live_items have no work
     const RequestInfo *reqs;
     const int32_t *kv_indices;
     const uint16_t *q;

@@ -34,7 +34,7 @@ PKV_F32 = 1
 EXPORTED = ("pkv_plan_create", "pkv_run", "pkv_merge_state", "pkv_plan_destroy",
             "pkv_plan_get_info", "pkv_plan_device_status", "pkv_status_string",
             "pkv_last_error", "pkv_abi_version", "pkv_plan_set_timing_events",
-            "pkv_decode_noalloc")
+            "pkv_decode_noalloc", "pkv_plan_create_capturable", "pkv_plan_update")
 
 
 class PkvError(RuntimeError):
@@ -63,6 +63,14 @@ class PlanDesc(ctypes.Structure):
         ("fixed_split_size", ctypes.c_int32),
         ("disable_split_kv", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
+    ]
+
+
+class PlanCaps(ctypes.Structure):
+    _fields_ = [
+        ("max_batch", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("max_total_q", ctypes.c_int64),
     ]
 
 
@@ -116,6 +124,11 @@ def load_library(path: Optional[str] = None):
         lib.pkv_plan_set_timing_events.restype = ctypes.c_int
         lib.pkv_decode_noalloc.argtypes = [ctypes.POINTER(PlanDesc), vp, vp, vp, vp, vp, vp]
         lib.pkv_decode_noalloc.restype = ctypes.c_int
+        lib.pkv_plan_create_capturable.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(PlanDesc),
+                                                    ctypes.POINTER(PlanCaps), vp]
+        lib.pkv_plan_create_capturable.restype = ctypes.c_int
+        lib.pkv_plan_update.argtypes = [vp, ctypes.POINTER(PlanDesc), vp]
+        lib.pkv_plan_update.restype = ctypes.c_int
         lib.pkv_abi_version.argtypes = []
         lib.pkv_abi_version.restype = ctypes.c_int
         _lib = lib
@@ -158,7 +171,10 @@ class Plan:
                  num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                  num_pages: int, window_left: int = -1, causal: bool = True,
                  sm_scale: Optional[float] = None, qo_indptr=None, q_start=None,
-                 fixed_split_size: int = -1, disable_split_kv: bool = False, stream=None):
+                 fixed_split_size: int = -1, disable_split_kv: bool = False, stream=None,
+                 capacity: Optional[dict] = None):
+        """capacity={"max_batch": B, "max_total_q": Q}: a capturable plan (its run may
+        be captured in a CUDA graph and replayed after update())."""
         self._lib = load_library()
         self._handle = ctypes.c_void_p()
         self.kind = kind
@@ -188,10 +204,39 @@ class Plan:
         d.fixed_split_size = int(fixed_split_size)
         d.disable_split_kv = 1 if disable_split_kv else 0
         d.dtype = PKV_BF16
-        _check(self._lib.pkv_plan_create(ctypes.byref(self._handle), ctypes.byref(d),
-                                         _stream_handle(stream)), "pkv_plan_create")
+        self._desc = d
+        if capacity is None:
+            _check(self._lib.pkv_plan_create(ctypes.byref(self._handle), ctypes.byref(d),
+                                             _stream_handle(stream)), "pkv_plan_create")
+        else:
+            caps = PlanCaps()
+            caps.max_batch = int(capacity["max_batch"])
+            caps.max_total_q = int(capacity.get("max_total_q", capacity["max_batch"]))
+            _check(self._lib.pkv_plan_create_capturable(ctypes.byref(self._handle), ctypes.byref(d),
+                                                        ctypes.byref(caps), _stream_handle(stream)),
+                   "pkv_plan_create_capturable")
         self.num_qo_heads = int(num_qo_heads)
         self.head_dim = int(head_dim)
+        self.info = self.get_info()
+
+    def update(self, *, kv_indptr, kv_last_page_len, qo_indptr=None, q_start=None,
+               fixed_split_size: int = -1, disable_split_kv: bool = False, stream=None):
+        """Re-plan a capturable plan for a new batch (same heads, window, page pool and
+        kv_indices tensor, whose contents the caller has rewritten)."""
+        kv_indptr = _host_i32(kv_indptr)
+        kv_last_page_len = _host_i32(kv_last_page_len)
+        qo_indptr = _host_i32(qo_indptr)
+        q_start = _host_i32(q_start)
+        d = PlanDesc.from_buffer_copy(self._desc)
+        d.batch_size = len(kv_last_page_len)
+        d.qo_indptr = None if qo_indptr is None else qo_indptr.ctypes.data
+        d.kv_indptr = kv_indptr.ctypes.data
+        d.kv_last_page_len = kv_last_page_len.ctypes.data
+        d.q_start = None if q_start is None else q_start.ctypes.data
+        d.fixed_split_size = int(fixed_split_size)
+        d.disable_split_kv = 1 if disable_split_kv else 0
+        _check(self._lib.pkv_plan_update(self._handle, ctypes.byref(d), _stream_handle(stream)),
+               "pkv_plan_update")
         self.info = self.get_info()
 
     def get_info(self) -> dict:

@@ -36,7 +36,7 @@ def test_header_declares_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_entry_points():
         assert hasattr(lib, name), name
-    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -129,3 +129,17 @@ def test_merge_state_rejects_bad_arguments(lib):
     assert lib.pkv_merge_state(ctypes.c_void_p(0x1008), p, p, p, p, p, 4, 2, 128, 0, None) == \
         pkv.PKV_ERR_INVALID_ARG  # misaligned
     assert lib.pkv_merge_state(p, p, p, p, p, p, 0, 2, 128, 0, None) == pkv.PKV_OK  # empty: no launch
+
+
+def test_capturable_entry_points_reject_bad_arguments_on_the_host(lib):
+    d, keep = _desc()
+    out = ctypes.c_void_p()
+    assert lib.pkv_plan_create_capturable(ctypes.byref(out), ctypes.byref(d), None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert out.value is None
+    caps = pkv.PlanCaps()
+    caps.max_batch = 1  # below the batch of 2
+    caps.max_total_q = 100
+    assert lib.pkv_plan_create_capturable(ctypes.byref(out), ctypes.byref(d), ctypes.byref(caps),
+                                          None) == pkv.PKV_ERR_INVALID_ARG
+    assert b"capacity" in lib.pkv_last_error()
+    assert lib.pkv_plan_update(None, ctypes.byref(d), None) == pkv.PKV_ERR_INVALID_ARG
