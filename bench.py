@@ -384,7 +384,32 @@ def run_ours(args, rank, world):
     return line
 
 
-EXTRA = ("swa_prefill_p1", "swa_prefill_p16", "extend_prefix", "long_decode")
+EXTRA = ("swa_prefill_p1", "swa_prefill_p16", "extend_prefix", "extend_ragged", "long_decode")
+
+
+def bench_prefill_ragged(pkv, w, steps, warmup, flush):
+    """The workload's K/V packed contiguously, request after request, through the
+    ragged (non-paged) prefill path."""
+    P = w.page_size
+    idx = torch.as_tensor(w.kv_indices.astype(np.int64), device="cuda")
+    kp = w.k_cache[idx].reshape(-1, w.num_kv_heads, w.head_dim)
+    vp = w.v_cache[idx].reshape(-1, w.num_kv_heads, w.head_dim)
+    lens = [int(x) for x in w.kv_lens]
+    sel = torch.cat([torch.arange(int(w.kv_indptr[b]) * P, int(w.kv_indptr[b]) * P + lens[b])
+                     for b in range(w.batch)]).to("cuda")
+    k, v = kp[sel].contiguous(), vp[sel].contiguous()
+    del kp, vp
+    kv_indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    plan = pkv.Plan(kind="prefill_ragged", qo_indptr=w.qo_indptr, kv_indptr=kv_indptr,
+                    num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                    window_left=w.window_left, causal=w.causal, sm_scale=w.sm_scale, q_start=w.q_start)
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.q.shape[0], w.q.shape[1], dtype=torch.float32, device="cuda")
+    step_ms, kern_ms = _timed_runs([(plan, (w.q, k, v, out, lse))], steps, warmup, flush)
+    flops = workcount.attention_flops(w)
+    t = sum(kern_ms) / steps
+    return {"tflops": flops / (t * 1e-3) / 1e12, "kernel_ms": t, "algorithmic_gflop": flops / 1e9,
+            "work_items": plan.info["num_work_items"]}
 
 
 def extra_workloads(pkv, args, peaks, flush, only=None):
@@ -404,6 +429,13 @@ def extra_workloads(pkv, args, peaks, flush, only=None):
         r = bench_prefill(pkv, w, steps, 3, flush)
         r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
         res["extend_prefix_16req_W4095"] = r
+        del w
+        torch.cuda.empty_cache()
+    if want("extend_ragged"):
+        w = wl.extend_with_prefix(device="cuda")
+        r = bench_prefill_ragged(pkv, w, steps, 3, flush)
+        r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
+        res["extend_prefix_16req_W4095_ragged_kv"] = r
         del w
         torch.cuda.empty_cache()
     for W in (wl.LONG_DECODE_WINDOWS if want("long_decode") else ()):

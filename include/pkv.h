@@ -74,8 +74,15 @@ typedef enum pkv_status {
 } pkv_status;
 
 typedef enum pkv_kind {
-    PKV_PREFILL = 0, /* ragged query rows per request (extend over a cached prefix) */
-    PKV_DECODE = 1   /* exactly one query row per request */
+    PKV_PREFILL = 0,        /* ragged query rows per request (extend over a cached prefix) */
+    PKV_DECODE = 1,         /* exactly one query row per request */
+    PKV_PREFILL_RAGGED = 2  /* ragged query rows against contiguous, non-paged K/V: k_cache
+                               and v_cache passed to pkv_run are [total_kv, H_kv, d] with the
+                               keys of request b at rows [kv_indptr[b], kv_indptr[b+1]);
+                               kv_indptr counts tokens; kv_indices, kv_last_page_len,
+                               page_size and num_pages are ignored (the ragged extend of
+                               flashinfer_backend.py forward_extend, whose result is merged
+                               with a paged prefix's by pkv_merge_state). Not capturable. */
 } pkv_kind;
 
 typedef enum pkv_dtype {

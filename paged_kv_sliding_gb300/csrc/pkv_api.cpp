@@ -66,6 +66,7 @@ struct pkv_plan {
     cudaEvent_t staging_done[2] = {nullptr, nullptr};
     int staging_next = 0;
     int32_t *d_live = nullptr;  // live work items (capturable decode launches exit above it)
+    int64_t total_kv = 0;       // ragged prefill: rows of the contiguous K/V
     int decode_tile = 64;  // decode: KV tokens per stage of the kernel
     int64_t total_q = 0;
     const int32_t *kv_indices = nullptr;  // borrowed device pointer
@@ -92,15 +93,16 @@ int validate(const pkv_plan_desc *d, std::vector<HostRequest> &reqs)
 {
     if (!d)
         return fail(PKV_ERR_INVALID_ARG, "desc is NULL");
-    if (d->kind != PKV_PREFILL && d->kind != PKV_DECODE)
-        return fail(PKV_ERR_INVALID_ARG, "kind %d is neither PKV_PREFILL nor PKV_DECODE", d->kind);
+    if (d->kind != PKV_PREFILL && d->kind != PKV_DECODE && d->kind != PKV_PREFILL_RAGGED)
+        return fail(PKV_ERR_INVALID_ARG, "kind %d is not a pkv_kind", d->kind);
+    const bool ragged = d->kind == PKV_PREFILL_RAGGED;
     if (d->batch_size < 0)
         return fail(PKV_ERR_INVALID_ARG, "batch_size %d < 0", d->batch_size);
     const int B = d->batch_size;
-    if (!d->kv_indptr || !d->kv_last_page_len)
-        return fail(PKV_ERR_INVALID_ARG, "kv_indptr and kv_last_page_len are required");
-    if (d->kind == PKV_PREFILL && !d->qo_indptr)
-        return fail(PKV_ERR_INVALID_ARG, "PKV_PREFILL needs qo_indptr");
+    if (!d->kv_indptr || (!ragged && !d->kv_last_page_len))
+        return fail(PKV_ERR_INVALID_ARG, "kv_indptr%s required", ragged ? " is" : " and kv_last_page_len are");
+    if (d->kind != PKV_DECODE && !d->qo_indptr)
+        return fail(PKV_ERR_INVALID_ARG, "prefill plans need qo_indptr");
     if (d->num_qo_heads <= 0 || d->num_kv_heads <= 0)
         return fail(PKV_ERR_INVALID_ARG, "head counts must be positive (%d, %d)", d->num_qo_heads,
                     d->num_kv_heads);
@@ -109,7 +111,7 @@ int validate(const pkv_plan_desc *d, std::vector<HostRequest> &reqs)
                     d->num_qo_heads, d->num_kv_heads);
     if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256)
         return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", d->head_dim);
-    if (d->page_size <= 0)
+    if (!ragged && d->page_size <= 0)
         return fail(PKV_ERR_INVALID_ARG, "page_size %d <= 0", d->page_size);
     if (d->num_pages < 0)
         return fail(PKV_ERR_INVALID_ARG, "num_pages %d < 0", d->num_pages);
@@ -119,30 +121,33 @@ int validate(const pkv_plan_desc *d, std::vector<HostRequest> &reqs)
         return fail(PKV_ERR_INVALID_ARG, "sm_scale is not finite");
     if (!(d->sm_scale > 0.f))
         return fail(PKV_ERR_UNSUPPORTED, "sm_scale must be positive");
-    if (d->kind == PKV_PREFILL &&
+    if (d->kind != PKV_DECODE &&
         d->num_qo_heads / d->num_kv_heads > kPrefillRows)
         return fail(PKV_ERR_UNSUPPORTED, "query-head group %d exceeds %d",
                     d->num_qo_heads / d->num_kv_heads, kPrefillRows);
     if (d->kv_indptr[0] != 0)
         return fail(PKV_ERR_INVALID_ARG, "kv_indptr[0] = %d, expected 0", d->kv_indptr[0]);
-    if (d->kind == PKV_PREFILL && d->qo_indptr[0] != 0)
+    if (d->kind != PKV_DECODE && d->qo_indptr[0] != 0)
         return fail(PKV_ERR_INVALID_ARG, "qo_indptr[0] = %d, expected 0", d->qo_indptr[0]);
-    if (B > 0 && d->kv_indptr[B] > 0 && !d->kv_indices)
+    if (!ragged && B > 0 && d->kv_indptr[B] > 0 && !d->kv_indices)
         return fail(PKV_ERR_INVALID_ARG, "kv_indices is NULL but the batch holds pages");
     reqs.resize(B);
     for (int b = 0; b < B; ++b) {
         int64_t np = (int64_t)d->kv_indptr[b + 1] - d->kv_indptr[b];
         if (np < 0)
             return fail(PKV_ERR_INVALID_ARG, "kv_indptr decreases at request %d", b);
-        int64_t last = d->kv_last_page_len[b];
-        if (np > 0 && (last < 1 || last > d->page_size))
-            return fail(PKV_ERR_INVALID_ARG, "kv_last_page_len[%d] = %lld outside [1, %d]", b,
-                        (long long)last, d->page_size);
-        int64_t kv_len = np > 0 ? (np - 1) * d->page_size + last : 0;
+        int64_t kv_len = np;  // ragged: kv_indptr counts tokens
+        if (!ragged) {
+            int64_t last = d->kv_last_page_len[b];
+            if (np > 0 && (last < 1 || last > d->page_size))
+                return fail(PKV_ERR_INVALID_ARG, "kv_last_page_len[%d] = %lld outside [1, %d]", b,
+                            (long long)last, d->page_size);
+            kv_len = np > 0 ? (np - 1) * d->page_size + last : 0;
+        }
         if (kv_len > INT32_MAX / 2)
             return fail(PKV_ERR_UNSUPPORTED, "request %d holds %lld tokens", b, (long long)kv_len);
         int64_t qo_begin, qo_len;
-        if (d->kind == PKV_PREFILL) {
+        if (d->kind != PKV_DECODE) {
             qo_begin = d->qo_indptr[b];
             qo_len = (int64_t)d->qo_indptr[b + 1] - d->qo_indptr[b];
             if (qo_len < 0)
@@ -306,11 +311,14 @@ void build_schedule(const pkv_plan_desc &d, const std::vector<HostRequest> &reqs
     int mask_mode = causal ? (W >= 0 ? kMaskCausalWindow : kMaskCausal)
                            : (W >= 0 ? kMaskWindow : kMaskNone);
 
-    if (d.kind == PKV_PREFILL) {
+    if (d.kind != PKV_DECODE) {
         const int T = prefill_kv_tile(d.head_dim);
         const int tq = prefill_tokens_per_cta(d.head_dim, group);
-        const int64_t kv_align =
-            prefill_pp_tma_page_size(d.page_size, d.head_dim) ? std::min(d.page_size, T) : 1;
+        // Ragged K/V: a TMA box may start at any row. Pages: at a page (TMA page
+        // boxes) or anywhere (cp.async gathers).
+        const int64_t kv_align = d.kind == PKV_PREFILL_RAGGED                        ? 1
+                                 : prefill_pp_tma_page_size(d.page_size, d.head_dim) ? std::min(d.page_size, T)
+                                                                                     : 1;
         for (int b = 0; b < B; ++b) {
             const HostRequest &r = reqs[b];
             for (int64_t t0 = 0; t0 < r.qo_len; t0 += tq) {
@@ -449,7 +457,7 @@ Caps caps_of(const pkv_plan_desc &d, const Schedule &sc)
     Caps c;
     c.batch = d.batch_size;
     c.total_q = sc.total_q;
-    c.items = d.kind == PKV_PREFILL ? (int64_t)sc.p_items.size() : (int64_t)sc.d_items.size();
+    c.items = d.kind != PKV_DECODE ? (int64_t)sc.p_items.size() : (int64_t)sc.d_items.size();
     c.lists = sc.cta_items.empty() ? 0 : (int64_t)sc.cta_items.size() - 1;
     c.partials = sc.num_partials;
     c.counters = sc.num_counters;
@@ -461,7 +469,7 @@ Caps caps_for_capacity(const pkv_plan_desc &d, const pkv_plan_caps &cap, int n_s
     const int group = d.num_qo_heads / d.num_kv_heads;
     Caps c;
     c.batch = cap.max_batch;
-    if (d.kind == PKV_PREFILL) {
+    if (d.kind != PKV_DECODE) {
         const int64_t tq = prefill_tokens_per_cta(d.head_dim, group);
         c.total_q = cap.max_total_q;
         c.items = (int64_t)d.num_kv_heads * ((cap.max_total_q + tq - 1) / tq + cap.max_batch);
@@ -484,7 +492,7 @@ struct Layout {
 
 Layout layout_for(const pkv_plan_desc &d, const Caps &c)
 {
-    const size_t item_bytes = d.kind == PKV_PREFILL ? sizeof(PrefillItem) : sizeof(DecodeItem);
+    const size_t item_bytes = d.kind != PKV_DECODE ? sizeof(PrefillItem) : sizeof(DecodeItem);
     size_t off = 0;
     auto carve = [&](size_t bytes) {
         size_t at = off;
@@ -510,12 +518,12 @@ void fill_image(const pkv_plan_desc &d, const Schedule &sc, const Layout &l, uin
 {
     std::memset(img, 0, l.upload);
     std::memcpy(img + l.reqs, sc.reqs.data(), sizeof(RequestInfo) * sc.reqs.size());
-    if (d.kind == PKV_PREFILL)
+    if (d.kind != PKV_DECODE)
         std::memcpy(img + l.items, sc.p_items.data(), sizeof(PrefillItem) * sc.p_items.size());
     else
         std::memcpy(img + l.items, sc.d_items.data(), sizeof(DecodeItem) * sc.d_items.size());
     std::memcpy(img + l.cta, sc.cta_items.data(), sizeof(int32_t) * sc.cta_items.size());
-    const int32_t live = d.kind == PKV_PREFILL ? (int32_t)sc.p_items.size() : (int32_t)sc.d_items.size();
+    const int32_t live = d.kind != PKV_DECODE ? (int32_t)sc.p_items.size() : (int32_t)sc.d_items.size();
     std::memcpy(img + l.live, &live, sizeof(live));
 }
 
@@ -555,10 +563,12 @@ int create_plan(pkv_plan **out, const pkv_plan_desc *desc, const pkv_plan_caps *
         return st;
     const pkv_plan_desc &d = *desc;
     const bool capturable = capacity != nullptr;
+    if (capturable && d.kind == PKV_PREFILL_RAGGED)
+        return fail(PKV_ERR_UNSUPPORTED, "ragged plans are not capturable (the K/V row count is baked into a launch)");
     if (capturable && (capacity->max_batch < d.batch_size || capacity->max_batch < 1 ||
-                       (d.kind == PKV_PREFILL && capacity->max_total_q < 1)))
+                       (d.kind != PKV_DECODE && capacity->max_total_q < 1)))
         return fail(PKV_ERR_INVALID_ARG, "capacity: max_batch must be >= 1 and >= batch_size%s",
-                    d.kind == PKV_PREFILL ? ", max_total_q >= 1" : "");
+                    d.kind != PKV_DECODE ? ", max_total_q >= 1" : "");
     cudaStream_t stream = (cudaStream_t)stream_;
     int device = 0;
     cudaError_t ce = cudaGetDevice(&device);
@@ -618,11 +628,12 @@ int create_plan(pkv_plan **out, const pkv_plan_desc *desc, const pkv_plan_caps *
     plan->n_sm = n_sm;
     plan->capturable = capturable;
     plan->mask_mode = sc.mask_mode;
-    plan->num_items = (int)(d.kind == PKV_PREFILL ? sc.p_items.size() : sc.d_items.size());
+    plan->num_items = (int)(d.kind != PKV_DECODE ? sc.p_items.size() : sc.d_items.size());
     plan->num_partials = sc.num_partials;
     plan->num_ctas = sc.cta_items.empty() ? 0 : (int)sc.cta_items.size() - 1;
     plan->decode_tile = sc.decode_tile;
     plan->total_q = sc.total_q;
+    plan->total_kv = d.batch_size > 0 ? d.kv_indptr[d.batch_size] : 0;
     plan->cap_items = caps.items;
     plan->cap_total_q = caps.total_q;
     plan->cap_batch = caps.batch;
@@ -689,7 +700,7 @@ int pkv_plan_update(pkv_plan *plan, const pkv_plan_desc *desc, void *stream_)
         return fail(PKV_ERR_INVALID_ARG, "plan was made on device %d, current device is %d", plan->device, cur);
     Schedule sc;
     build_schedule(d, reqs, plan->device, true, plan->decode_tile, sc);
-    const int64_t items = d.kind == PKV_PREFILL ? (int64_t)sc.p_items.size() : (int64_t)sc.d_items.size();
+    const int64_t items = d.kind != PKV_DECODE ? (int64_t)sc.p_items.size() : (int64_t)sc.d_items.size();
     if (sc.total_q > plan->cap_total_q || items > plan->cap_items)
         return fail(PKV_ERR_UNSUPPORTED, "the batch needs %lld query rows and %lld work items, the capacity is %lld "
                     "and %lld", (long long)sc.total_q, (long long)items, (long long)plan->cap_total_q,
@@ -871,6 +882,13 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.num_pages = d.num_pages;
     p.window_left = d.window_left;
     p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
+    p.ragged = d.kind == PKV_PREFILL_RAGGED ? 1 : 0;
+    p.total_kv = (int32_t)plan->total_kv;
+    if (p.ragged) {
+        p.page_size = 1;
+        p.page_shift = 0;
+        p.num_pages = (int32_t)plan->total_kv;
+    }
     if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
         return cuda_fail(ce, "cudaEventRecord");
     ce = launch_prefill_pp(p, d.head_dim, plan->mask_mode, plan->capturable ? plan->n_sm : plan->num_ctas, stream);

@@ -131,6 +131,8 @@ struct PrefillParams {
     int32_t window_left;
     int32_t total_q;         // rows of q (bound of the query tensor map)
     float sm_scale_log2;
+    int32_t ragged;          // 1: K/V are contiguous [total_kv, H_kv, d], kv_page_begin = token offset
+    int32_t total_kv;        // ragged: rows of K/V (bound of their tensor maps)
 };
 
 // Launchers (one per kernel family); return cudaGetLastError() of the launch.

@@ -89,7 +89,7 @@ struct PPBars {
     static constexpr int kCount = kDrain + 1;
 };
 
-template <int D, int MASK, bool TMA_KV>
+template <int D, int MASK, bool TMA_KV, bool RAGGED>
 __global__ void __launch_bounds__(384, 1)
     prefill_pp_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
@@ -449,6 +449,46 @@ __global__ void __launch_bounds__(384, 1)
             mbar_wait(bar(B::kDrain), 0, &no_abort, kWaitLimitPP);
         }
         __syncwarp();
+    } else if (RAGGED) {
+        // ------------------------------------------------------------ TMA producer, ragged K/V
+        // K/V rows of request b are rows kv_page_begin + j of a [total_kv, H_kv, d]
+        // tensor: one box per 64-column chunk of a tile, at any row. Rows past the
+        // request's keys are the next request's (finite, masked in S, so P = 0) or
+        // past the tensor's end (filled with zeros by the copy).
+        static_assert(!RAGGED || TMA_KV, "ragged K/V are loaded by TMA");
+        if (warp == 9 && lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            uint32_t n = 0;  // K/V ring position
+            bool okp = true;
+            for (int ii = item_lo; okp && ii < item_hi; ++ii) {
+                const PrefillItem it = p.items[ii];
+                const int n_tiles = it.kv_tiles;
+                if (n_tiles <= 0)
+                    continue;
+                const int row_base = p.reqs[it.req].kv_page_begin;
+                for (int j = 0; okp && j < n_tiles; ++j) {
+                    const int row0 = row_base + prefill_kv_key_at(it, j, T);
+                    const uint32_t full = bar(B::kFull + n % NS);  // K and V of the tile complete it
+                    for (int isv = 0; isv < 2; ++isv, ++n) {
+                        const int s = n % NS;
+                        if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP)) {
+                            okp = false;
+                            break;
+                        }
+                        if (isv == 0)
+                            mbar_arrive_expect_tx(full, 2u * T * Tr::kChunk * NCH);
+                        const void *tm = isv ? (const void *)&tm_v : (const void *)&tm_k;
+                        for (int c = 0; c < NCH; ++c)
+                            tma_load_4d(slot(s) + c * (T * Tr::kChunk), tm, c * 64, it.kv_head, row0, 0, full);
+                    }
+                }
+            }
+            if (!okp) {
+                record_status(p.status, PKV_ERR_TIMEOUT);
+                abort_flag = 1;
+            }
+        }
     } else if (TMA_KV) {
         // ------------------------------------------------------------ TMA producer
         if (warp == 9) {
@@ -692,32 +732,32 @@ bool encode_4d(CUtensorMap *m, const void *base, const cuuint64_t dims[4], const
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int MASK, bool TMA_KV>
+template <int D, int MASK, bool TMA_KV, bool RAGGED>
 cudaError_t launch_pp_dmt(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                           const CUtensorMap &tv, int num_ctas, cudaStream_t s)
 {
     using Tr = PPTraits<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_pp_kernel<D, MASK, TMA_KV>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_pp_kernel<D, MASK, TMA_KV, RAGGED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kDynSmem);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    prefill_pp_kernel<D, MASK, TMA_KV><<<num_ctas, Tr::kThreads, Tr::kDynSmem, s>>>(p, tq, tk, tv);
+    prefill_pp_kernel<D, MASK, TMA_KV, RAGGED><<<num_ctas, Tr::kThreads, Tr::kDynSmem, s>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
-template <int D, bool TMA_KV>
+template <int D, bool TMA_KV, bool RAGGED = false>
 cudaError_t launch_pp_dt(const PrefillParams &p, int mask_mode, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, int num_ctas, cudaStream_t s)
 {
     switch (mask_mode) {
-    case kMaskNone: return launch_pp_dmt<D, kMaskNone, TMA_KV>(p, tq, tk, tv, num_ctas, s);
-    case kMaskCausal: return launch_pp_dmt<D, kMaskCausal, TMA_KV>(p, tq, tk, tv, num_ctas, s);
-    case kMaskCausalWindow: return launch_pp_dmt<D, kMaskCausalWindow, TMA_KV>(p, tq, tk, tv, num_ctas, s);
-    case kMaskWindow: return launch_pp_dmt<D, kMaskWindow, TMA_KV>(p, tq, tk, tv, num_ctas, s);
+    case kMaskNone: return launch_pp_dmt<D, kMaskNone, TMA_KV, RAGGED>(p, tq, tk, tv, num_ctas, s);
+    case kMaskCausal: return launch_pp_dmt<D, kMaskCausal, TMA_KV, RAGGED>(p, tq, tk, tv, num_ctas, s);
+    case kMaskCausalWindow: return launch_pp_dmt<D, kMaskCausalWindow, TMA_KV, RAGGED>(p, tq, tk, tv, num_ctas, s);
+    case kMaskWindow: return launch_pp_dmt<D, kMaskWindow, TMA_KV, RAGGED>(p, tq, tk, tv, num_ctas, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -737,7 +777,7 @@ int prefill_kv_tile(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mode, int num_ctas, cudaStream_t s)
 {
     const int g = p.group, tq = p.tokens_per_tile, Hkv = p.num_kv_heads, P = p.page_size;
-    const bool tma_kv = prefill_pp_tma_page_size(P, head_dim);
+    const bool tma_kv = p.ragged || prefill_pp_tma_page_size(P, head_dim);
     const int T = prefill_kv_tile(head_dim);
     CUtensorMap tm_q{}, tm_k{}, tm_v{};
     {
@@ -748,6 +788,22 @@ cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mod
         const cuuint32_t box[4] = {64, (cuuint32_t)g, 1, (cuuint32_t)tq};
         if (!encode_4d(&tm_q, p.q, dims, strides, box))
             return cudaErrorInvalidValue;
+    }
+    if (p.ragged) {
+        // [total_kv][H_kv][d] viewed as 4-D with a unit outer dimension; box (64, 1, T, 1)
+        const cuuint64_t rows = (cuuint64_t)(p.total_kv > 0 ? p.total_kv : 1);
+        const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)Hkv, rows, 1};
+        const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)Hkv * head_dim * 2,
+                                       rows * Hkv * head_dim * 2};
+        const cuuint32_t box[4] = {64, 1, (cuuint32_t)T, 1};
+        if (!encode_4d(&tm_k, p.k_cache, dims, strides, box) || !encode_4d(&tm_v, p.v_cache, dims, strides, box))
+            return cudaErrorInvalidValue;
+        switch (head_dim) {
+        case 64: return launch_pp_dt<64, true, true>(p, mask_mode, tm_q, tm_k, tm_v, num_ctas, s);
+        case 128: return launch_pp_dt<128, true, true>(p, mask_mode, tm_q, tm_k, tm_v, num_ctas, s);
+        case 256: return launch_pp_dt<256, true, true>(p, mask_mode, tm_q, tm_k, tm_v, num_ctas, s);
+        default: return cudaErrorInvalidValue;
+        }
     }
     if (tma_kv) {
         const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)Hkv, (cuuint64_t)P,

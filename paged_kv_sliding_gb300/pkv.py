@@ -28,6 +28,7 @@ PKV_ERR_TIMEOUT = 6
 
 PKV_PREFILL = 0
 PKV_DECODE = 1
+PKV_PREFILL_RAGGED = 2
 PKV_BF16 = 0
 PKV_F32 = 1
 
@@ -167,27 +168,38 @@ class Plan:
     Host index arrays are copied by the library.
     """
 
-    def __init__(self, *, kind: str, kv_indptr, kv_indices: torch.Tensor, kv_last_page_len,
-                 num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
-                 num_pages: int, window_left: int = -1, causal: bool = True,
+    def __init__(self, *, kind: str, kv_indptr, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+                 kv_indices: Optional[torch.Tensor] = None, kv_last_page_len=None,
+                 page_size: int = 1, num_pages: int = 0, window_left: int = -1, causal: bool = True,
                  sm_scale: Optional[float] = None, qo_indptr=None, q_start=None,
                  fixed_split_size: int = -1, disable_split_kv: bool = False, stream=None,
                  capacity: Optional[dict] = None):
-        """capacity={"max_batch": B, "max_total_q": Q}: a capturable plan (its run may
+        """kind: "prefill", "decode" or "prefill_ragged" (K/V passed to run() are
+        contiguous [total_kv, H_kv, d]; kv_indptr counts tokens; no page table).
+        capacity={"max_batch": B, "max_total_q": Q}: a capturable plan (its run may
         be captured in a CUDA graph and replayed after update())."""
         self._lib = load_library()
         self._handle = ctypes.c_void_p()
         self.kind = kind
         kv_indptr = _host_i32(kv_indptr)
+        ragged = kind == "prefill_ragged"
+        if kv_last_page_len is None:
+            if not ragged:
+                raise ValueError("kv_last_page_len is required for paged plans")
+            kv_last_page_len = np.ones(len(kv_indptr) - 1, dtype=np.int32)
         kv_last_page_len = _host_i32(kv_last_page_len)
         qo_indptr = _host_i32(qo_indptr)
         q_start = _host_i32(q_start)
+        if kv_indices is None:
+            if not ragged:
+                raise ValueError("kv_indices is required for paged plans")
+            kv_indices = torch.zeros(0, dtype=torch.int32, device="cuda")
         if kv_indices.dtype != torch.int32 or not kv_indices.is_cuda:
             raise ValueError("kv_indices must be a device int32 tensor")
         self._kv_indices = kv_indices.contiguous()
         d = PlanDesc()
-        d.kind = PKV_DECODE if kind == "decode" else PKV_PREFILL
-        d.batch_size = len(kv_last_page_len)
+        d.kind = {"decode": PKV_DECODE, "prefill": PKV_PREFILL, "prefill_ragged": PKV_PREFILL_RAGGED}[kind]
+        d.batch_size = len(kv_indptr) - 1
         d.qo_indptr = None if qo_indptr is None else qo_indptr.ctypes.data
         d.kv_indptr = kv_indptr.ctypes.data
         d.kv_last_page_len = kv_last_page_len.ctypes.data

@@ -143,3 +143,29 @@ def test_capturable_entry_points_reject_bad_arguments_on_the_host(lib):
                                           None) == pkv.PKV_ERR_INVALID_ARG
     assert b"capacity" in lib.pkv_last_error()
     assert lib.pkv_plan_update(None, ctypes.byref(d), None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_ragged_desc_validation_on_the_host(lib):
+    qo = np.array([0, 3, 5], dtype=np.int32)
+    kv = np.array([0, 7, 9], dtype=np.int32)  # tokens
+    d = pkv.PlanDesc()
+    d.kind = pkv.PKV_PREFILL_RAGGED
+    d.batch_size = 2
+    d.qo_indptr = qo.ctypes.data
+    d.kv_indptr = kv.ctypes.data
+    d.kv_last_page_len = None  # not needed for ragged K/V
+    d.kv_indices = None
+    d.num_qo_heads, d.num_kv_heads, d.head_dim = 4, 1, 64
+    d.page_size, d.num_pages = 0, 0  # ignored for ragged K/V
+    d.window_left, d.causal, d.sm_scale, d.dtype = 3, 1, 0.125, pkv.PKV_BF16
+    d.fixed_split_size, d.disable_split_kv = -1, 0
+    out = ctypes.c_void_p()
+    caps = pkv.PlanCaps()
+    caps.max_batch, caps.max_total_q = 4, 16
+    assert lib.pkv_plan_create_capturable(ctypes.byref(out), ctypes.byref(d), ctypes.byref(caps),
+                                          None) == pkv.PKV_ERR_UNSUPPORTED
+    bad = np.array([0, 7, 5], dtype=np.int32)  # decreasing token offsets
+    d.kv_indptr = bad.ctypes.data
+    assert lib.pkv_plan_create(ctypes.byref(out), ctypes.byref(d), None) == pkv.PKV_ERR_INVALID_ARG
+    d.kind = 7
+    assert lib.pkv_plan_create(ctypes.byref(out), ctypes.byref(d), None) == pkv.PKV_ERR_INVALID_ARG
