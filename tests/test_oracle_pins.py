@@ -393,3 +393,53 @@ def test_merge_state_closed_forms(oracle_lib):
     mv2, ms2 = oracle_lib.merge_state(vb, sb, va, sa)
     np.testing.assert_allclose(mv2, mv, atol=1e-15)
     np.testing.assert_allclose(ms2, ms, atol=1e-15)
+
+
+
+# ------------------------------------------------------------- kv_indices builder oracle
+
+def test_kv_indices_identity_table_gives_position_ranges():
+    from oracle.kv_indices import build_kv_indices
+    table = np.arange(5 * 100).reshape(5, 100)  # slot = row * 100 + position
+    indptr, idx = build_kv_indices(table, [3, 0, 4], [10, 0, 95], [4, 0, 5])
+    assert indptr.tolist() == [0, 4, 4, 9]
+    assert idx.tolist() == [310, 311, 312, 313, 495, 496, 497, 498, 499]
+
+
+def test_kv_indices_location_map_composes():
+    from oracle.kv_indices import build_kv_indices
+    rng = np.random.default_rng(4)
+    table = rng.permutation(3 * 64).reshape(3, 64)
+    loc = rng.permutation(3 * 64)
+    starts, lens, rows = [5, 0, 30], [20, 64, 0], [2, 1, 0]
+    _, plain = build_kv_indices(table, rows, starts, lens)
+    _, mapped = build_kv_indices(table, rows, starts, lens, loc_map=loc)
+    assert np.array_equal(mapped, loc[plain])
+    assert len(plain) == sum(lens)
+
+
+def test_window_trimmed_indices_equal_windowed_attention(oracle_lib):
+    """Decode over indices trimmed to the last W+1 keys (kv_start = seq_len -
+    min(seq_len, W+1), the pages' window-only paged wrapper) without a window
+    equals decode over all keys with the window (page size 1)."""
+    from oracle.kv_indices import build_kv_indices
+    rng = np.random.default_rng(6)
+    B, H, Hkv, d, W, ctx = 5, 4, 2, 16, 9, 40
+    seq = rng.integers(1, ctx, size=B)
+    table = rng.permutation(B * ctx).reshape(B, ctx).astype(np.int32)  # token slots
+    k = torch.randn(B * ctx, 1, Hkv, d, dtype=torch.float64).to(torch.bfloat16)
+    v = torch.randn(B * ctx, 1, Hkv, d, dtype=torch.float64).to(torch.bfloat16)
+    q = torch.randn(B, H, d, dtype=torch.float64).to(torch.bfloat16)
+    rows = np.arange(B)
+    kw = dict(num_qo_heads=H, num_kv_heads=Hkv, head_dim=d, page_size=1, causal=True,
+              sm_scale=0.25, q=q, k_cache=k, v_cache=v, qo_indptr=np.arange(B + 1, dtype=np.int32),
+              num_pages=B * ctx)
+    ind_full, idx_full = build_kv_indices(table, rows, np.zeros(B), seq)
+    o_full, l_full = oracle_lib.attention(kv_indptr=ind_full, kv_indices=idx_full,
+                                          kv_last_page_len=np.ones(B, dtype=np.int32), window_left=W, **kw)
+    trim = np.minimum(seq, W + 1)
+    ind_t, idx_t = build_kv_indices(table, rows, seq - trim, trim)
+    o_t, l_t = oracle_lib.attention(kv_indptr=ind_t, kv_indices=idx_t,
+                                    kv_last_page_len=np.ones(B, dtype=np.int32), window_left=-1, **kw)
+    np.testing.assert_allclose(o_t, o_full, atol=1e-12)
+    np.testing.assert_allclose(l_t, l_full, atol=1e-12)
