@@ -270,6 +270,33 @@ PKV_API const char *pkv_status_string(int status);
 /* Reason for the last failure on the calling thread ("" if none). */
 PKV_API const char *pkv_last_error(void);
 
+/*
+ * pkv_build_kv_indices: build a batch's kv_indptr and kv_indices ON THE DEVICE from a
+ * request-to-slot table, so that the page table of a captured plan can be rebuilt
+ * between replays without a host round trip (sglang flashinfer_backend.py,
+ * call_begin_forward: kv_indptr[1:bs+1] = cumsum(paged_kernel_lens), the
+ * create_flashinfer_kv_indices_triton gather from kv_start_idx on, and the
+ * sliding-window pool's translate_loc_from_full_to_swa):
+ *   kv_indptr[0] = 0, kv_indptr[b+1] = kv_indptr[b] + kv_lens[b]
+ *   kv_indices[kv_indptr[b] + j] = req_to_token[req_pool_indices[b] * row_stride + kv_start[b] + j]
+ *   then, if loc_map != NULL: kv_indices[i] = loc_map[kv_indices[i]]
+ * The entries are whatever the table holds (token slots for page size 1, page ids
+ * otherwise). All pointers are DEVICE int32: req_to_token [num_rows, row_stride]
+ * (row-major), req_pool_indices / kv_start / kv_lens [batch_size], loc_map
+ * [loc_map_len] or NULL, kv_indptr [batch_size + 1] (written), kv_indices
+ * [kv_indices_capacity] (written), status: NULL or a device word in which a bounds
+ * violation on the device (a row, start or map entry out of range, a negative length,
+ * or more indices than kv_indices_capacity) is recorded as PKV_ERR_DEVICE_BOUNDS, the
+ * offending request or entry being skipped (map misses are written as -1).
+ * Asynchronous on `stream` (two kernel launches), allocates nothing; capturable.
+ * Returns PKV_OK, PKV_ERR_INVALID_ARG (NULL or negative arguments) or PKV_ERR_CUDA.
+ */
+PKV_API int pkv_build_kv_indices(const int32_t *req_to_token, int32_t num_rows, int64_t row_stride,
+                                 const int32_t *req_pool_indices, const int32_t *kv_start, const int32_t *kv_lens,
+                                 int32_t batch_size, const int32_t *loc_map, int64_t loc_map_len,
+                                 int32_t *kv_indptr, int32_t *kv_indices, int64_t kv_indices_capacity,
+                                 int32_t *status, void *stream);
+
 /* PKV_ABI_VERSION of the loaded library. */
 PKV_API int pkv_abi_version(void);
 

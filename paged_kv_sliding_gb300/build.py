@@ -22,7 +22,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
 
 SOURCES = ["pkv_api.cpp", "pkv_decode.cu", "pkv_merge.cu", "pkv_prefill.cu",
-           "pkv_noalloc.cu"]
+           "pkv_noalloc.cu", "pkv_indices.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -35,7 +35,8 @@ PKV_F32 = 1
 EXPORTED = ("pkv_plan_create", "pkv_run", "pkv_merge_state", "pkv_plan_destroy",
             "pkv_plan_get_info", "pkv_plan_device_status", "pkv_status_string",
             "pkv_last_error", "pkv_abi_version", "pkv_plan_set_timing_events",
-            "pkv_decode_noalloc", "pkv_plan_create_capturable", "pkv_plan_update")
+            "pkv_decode_noalloc", "pkv_plan_create_capturable", "pkv_plan_update",
+            "pkv_build_kv_indices")
 
 
 class PkvError(RuntimeError):
@@ -130,6 +131,8 @@ def load_library(path: Optional[str] = None):
         lib.pkv_plan_create_capturable.restype = ctypes.c_int
         lib.pkv_plan_update.argtypes = [vp, ctypes.POINTER(PlanDesc), vp]
         lib.pkv_plan_update.restype = ctypes.c_int
+        lib.pkv_build_kv_indices.argtypes = [vp, i32, i64, vp, vp, vp, i32, vp, i64, vp, vp, i64, vp, vp]
+        lib.pkv_build_kv_indices.restype = ctypes.c_int
         lib.pkv_abi_version.argtypes = []
         lib.pkv_abi_version.restype = ctypes.c_int
         _lib = lib
@@ -293,6 +296,33 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def build_kv_indices(req_to_token: torch.Tensor, req_pool_indices: torch.Tensor, kv_start: torch.Tensor,
+                     kv_lens: torch.Tensor, loc_map: Optional[torch.Tensor] = None, capacity: Optional[int] = None,
+                     kv_indptr: Optional[torch.Tensor] = None, kv_indices: Optional[torch.Tensor] = None,
+                     status: Optional[torch.Tensor] = None, stream=None):
+    """kv_indptr, kv_indices of a batch built on the device from a request-to-slot
+    table (device int32 tensors). `capacity` bounds kv_indices; when neither it nor
+    kv_indices is given it is read from kv_lens (one host read)."""
+    lib = load_library()
+    for t, name in ((req_to_token, "req_to_token"), (req_pool_indices, "req_pool_indices"),
+                    (kv_start, "kv_start"), (kv_lens, "kv_lens")):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+    B = kv_lens.numel()
+    if kv_indptr is None:
+        kv_indptr = torch.empty(B + 1, dtype=torch.int32, device=kv_lens.device)
+    if kv_indices is None:
+        if capacity is None:
+            capacity = int(kv_lens.clamp(min=0).sum().item())
+        kv_indices = torch.empty(max(1, capacity), dtype=torch.int32, device=kv_lens.device)
+    cap = kv_indices.numel() if capacity is None else min(int(capacity), kv_indices.numel())
+    _check(lib.pkv_build_kv_indices(_ptr(req_to_token), req_to_token.shape[0], req_to_token.shape[1],
+                                    _ptr(req_pool_indices), _ptr(kv_start), _ptr(kv_lens), B, _ptr(loc_map),
+                                    0 if loc_map is None else loc_map.numel(), _ptr(kv_indptr), _ptr(kv_indices),
+                                    cap, _ptr(status), _stream_handle(stream)), "pkv_build_kv_indices")
+    return kv_indptr, kv_indices
 
 
 def plan(**kw) -> Plan:
