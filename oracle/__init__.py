@@ -58,6 +58,10 @@ def _load():
             lib.pkv_oracle_attention.argtypes = [
                 i64, p, p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int,
                 ctypes.c_double, p, p, p, p, i64, p, p]
+            lib.pkv_oracle_attention_ext.restype = ctypes.c_int
+            lib.pkv_oracle_attention_ext.argtypes = [
+                i64, p, p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double, p, p, p, p, i64, p, p]
             lib.pkv_oracle_set_threads.restype = ctypes.c_int
             lib.pkv_oracle_set_threads.argtypes = [ctypes.c_int]
             lib.pkv_oracle_merge_state.restype = ctypes.c_int
@@ -93,7 +97,8 @@ def set_threads(n: int = 0) -> int:
 
 def attention(*, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, num_qo_heads,
               num_kv_heads, head_dim, page_size, window_left, causal, sm_scale, q, k_cache,
-              v_cache, q_start=None, rows=None, num_pages=None):
+              v_cache, q_start=None, rows=None, num_pages=None, logits_soft_cap=0.0, k_scale=1.0,
+              v_scale=1.0):
     """Reference attention in float64.
 
     q: bf16 [total_q, H_qo, d]; k_cache, v_cache: bf16 [num_pages, P, H_kv, d]
@@ -122,10 +127,11 @@ def attention(*, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, num_qo_head
         n = total_q
     out = np.zeros((n, num_qo_heads, head_dim), dtype=np.float64)
     lse = np.zeros((n, num_qo_heads), dtype=np.float64)
-    rc = lib.pkv_oracle_attention(
+    rc = lib.pkv_oracle_attention_ext(
         batch, _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len),
         _ptr(q_start), num_qo_heads, num_kv_heads, head_dim, page_size, int(num_pages),
-        int(window_left), int(bool(causal)), float(sm_scale), _ptr(qb), _ptr(kb), _ptr(vb),
+        int(window_left), int(bool(causal)), float(sm_scale), float(logits_soft_cap), float(k_scale),
+        float(v_scale), _ptr(qb), _ptr(kb), _ptr(vb),
         _ptr(sel), 0 if sel is None else len(sel), _ptr(out), _ptr(lse))
     if rc != OK:
         raise ValueError(f"oracle rejected its input (status {rc})")

@@ -35,6 +35,13 @@
  *     s_j = sm_scale * sum_c q[c] k_j[c]
  *     lse = ln sum_{j visible} exp(s_j)        (natural log of the scaled logits)
  *     out = sum_{j visible} exp(s_j - lse) v_j
+ *   pkv_oracle_attention_ext adds the three per-layer arguments the pages pass with
+ *   every attention call (flashinfer_backend.py forward_extend / forward_decode:
+ *   logits_soft_cap = layer.logit_cap, k_scale, v_scale), which the pages do not
+ *   define further; the readings taken (plainest ones):
+ *     s_j = cap * tanh(sm_scale * k_scale * q.k_j / cap)   (cap > 0; else no cap)
+ *     out = v_scale * sum_j exp(s_j - lse) v_j           (K and V dequantised by
+ *                                                          their scales)
  *   A row with no visible key has out = 0 and lse = -inf.
  *
  *   kv_len_b = (kv_indptr[b+1] - kv_indptr[b] - 1) * P + kv_last_page_len[b],
@@ -115,14 +122,23 @@ static int64_t request_of_row(const int32_t *qo_indptr, int64_t batch, int64_t r
  * Returns 0, PKV_ORACLE_BAD_ARG, or PKV_ORACLE_BAD_PAGE (a page id outside
  * [0, num_pages) met on a visible key).
  */
-int pkv_oracle_attention(int64_t batch, const int32_t *qo_indptr, const int32_t *kv_indptr,
-                         const int32_t *kv_indices, const int32_t *kv_last_page_len,
-                         const int32_t *q_start, int64_t num_qo_heads, int64_t num_kv_heads,
-                         int64_t head_dim, int64_t page_size, int64_t num_pages,
-                         int64_t window_left, int causal, double sm_scale, const uint16_t *q,
-                         const uint16_t *k_cache, const uint16_t *v_cache, const int64_t *rows,
-                         int64_t n_rows, double *out, double *lse)
+/* The logit of a key from its dot product with the query row. */
+static double logit_of(double dot, double scale, double cap)
 {
+    const double s = scale * dot;
+    return cap > 0.0 ? cap * tanh(s / cap) : s;
+}
+
+int pkv_oracle_attention_ext(int64_t batch, const int32_t *qo_indptr, const int32_t *kv_indptr,
+                             const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                             const int32_t *q_start, int64_t num_qo_heads, int64_t num_kv_heads,
+                             int64_t head_dim, int64_t page_size, int64_t num_pages,
+                             int64_t window_left, int causal, double sm_scale, double soft_cap,
+                             double k_scale, double v_scale, const uint16_t *q,
+                             const uint16_t *k_cache, const uint16_t *v_cache, const int64_t *rows,
+                             int64_t n_rows, double *out, double *lse)
+{
+    const double scale = sm_scale * k_scale;
     if (batch < 0 || num_kv_heads <= 0 || num_qo_heads <= 0 || head_dim <= 0 || page_size <= 0)
         return PKV_ORACLE_BAD_ARG;
     if (num_qo_heads % num_kv_heads != 0)
@@ -169,10 +185,10 @@ int pkv_oracle_attention(int64_t batch, const int32_t *qo_indptr, const int32_t 
             }
             const uint16_t *krow =
                 k_cache + ((page * page_size + j % page_size) * num_kv_heads + hk) * head_dim;
-            double s = 0.0;
+            double dot = 0.0;
             for (int64_t c = 0; c < head_dim; ++c)
-                s += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
-            s *= sm_scale;
+                dot += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
+            const double s = logit_of(dot, scale, soft_cap);
             if (s > m)
                 m = s;
             ++n_visible;
@@ -194,21 +210,34 @@ int pkv_oracle_attention(int64_t batch, const int32_t *qo_indptr, const int32_t 
             int64_t slot = (page * page_size + j % page_size) * num_kv_heads + hk;
             const uint16_t *krow = k_cache + slot * head_dim;
             const uint16_t *vrow = v_cache + slot * head_dim;
-            double s = 0.0;
+            double dot = 0.0;
             for (int64_t c = 0; c < head_dim; ++c)
-                s += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
-            s *= sm_scale;
+                dot += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
+            const double s = logit_of(dot, scale, soft_cap);
             double w = exp(s - m);
             denom += w;
             for (int64_t c = 0; c < head_dim; ++c)
                 o[c] += w * bf16_bits_to_double(vrow[c]);
         }
         for (int64_t c = 0; c < head_dim; ++c)
-            o[c] /= denom;
+            o[c] = v_scale * o[c] / denom;
         if (lse)
             lse[k_out * num_qo_heads + h] = m + log(denom);
     }
     return status;
+}
+
+int pkv_oracle_attention(int64_t batch, const int32_t *qo_indptr, const int32_t *kv_indptr,
+                         const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                         const int32_t *q_start, int64_t num_qo_heads, int64_t num_kv_heads,
+                         int64_t head_dim, int64_t page_size, int64_t num_pages,
+                         int64_t window_left, int causal, double sm_scale, const uint16_t *q,
+                         const uint16_t *k_cache, const uint16_t *v_cache, const int64_t *rows,
+                         int64_t n_rows, double *out, double *lse)
+{
+    return pkv_oracle_attention_ext(batch, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, q_start,
+                                    num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, window_left,
+                                    causal, sm_scale, 0.0, 1.0, 1.0, q, k_cache, v_cache, rows, n_rows, out, lse);
 }
 
 /*

@@ -443,3 +443,44 @@ def test_window_trimmed_indices_equal_windowed_attention(oracle_lib):
                                     kv_last_page_len=np.ones(B, dtype=np.int32), window_left=-1, **kw)
     np.testing.assert_allclose(o_t, o_full, atol=1e-12)
     np.testing.assert_allclose(l_t, l_full, atol=1e-12)
+
+
+
+# ------------------------------------------------- soft cap and K/V scales (oracle only)
+
+def _two_key_case(oracle_lib, s1, s2, **kw):
+    """One query (d = 1) against two keys with logits s1, s2 (sm_scale 1), V = (1, 0)."""
+    q = torch.tensor([[[1.0]]], dtype=torch.bfloat16)
+    k = torch.tensor([s1, s2], dtype=torch.float64).to(torch.bfloat16).reshape(2, 1, 1, 1)
+    v = torch.tensor([1.0, 0.0], dtype=torch.bfloat16).reshape(2, 1, 1, 1)
+    out, lse = oracle_lib.attention(qo_indptr=[0, 1], kv_indptr=[0, 2], kv_indices=[0, 1], kv_last_page_len=[1],
+                                    num_qo_heads=1, num_kv_heads=1, head_dim=1, page_size=1, window_left=-1,
+                                    causal=False, sm_scale=1.0, q=q, k_cache=k, v_cache=v, **kw)
+    return float(out[0, 0, 0]), float(lse[0, 0])
+
+
+def test_soft_cap_bounds_the_logits(oracle_lib):
+    """cap 1 saturates logits of +-1024 to +-1 exactly: the first key's weight is
+    e / (e + 1/e) and lse = ln(e + 1/e), whatever the raw logits."""
+    out, lse = _two_key_case(oracle_lib, 1024.0, -1024.0, logits_soft_cap=1.0)
+    assert abs(out - math.e / (math.e + 1 / math.e)) < 1e-15
+    assert abs(lse - math.log(math.e + 1 / math.e)) < 1e-15
+
+
+def test_soft_cap_vanishes_for_a_huge_cap(oracle_lib):
+    w = tiny_extend()
+    a = run_oracle(oracle_lib, w)
+    b = run_oracle(oracle_lib, w, logits_soft_cap=1e12)
+    np.testing.assert_allclose(b[0], a[0], atol=1e-12)
+    np.testing.assert_allclose(b[1], a[1], atol=1e-12)
+
+
+def test_kv_scales_equal_scaled_caches(oracle_lib):
+    """k_scale 2 equals doubling every K value (exact in bf16); v_scale 0.5 equals
+    halving every V value."""
+    w = tiny_extend()
+    a = run_oracle(oracle_lib, w, k_scale=2.0, v_scale=0.5, logits_soft_cap=3.0)
+    b = run_oracle(oracle_lib, w, k_cache=w.k_cache.cpu() * 2, v_cache=w.v_cache.cpu() * 0.5,
+                   logits_soft_cap=3.0)
+    np.testing.assert_allclose(a[0], b[0], atol=1e-14)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-14)
