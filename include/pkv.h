@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 2
+#define PKV_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define PKV_API __attribute__((visibility("default")))
@@ -121,6 +121,16 @@ typedef struct pkv_plan_desc {
                                         let the plan choose */
     int32_t disable_split_kv;        /* nonzero: one pass per (request, KV head) */
     int32_t dtype;                   /* pkv_dtype of q, caches and out: PKV_BF16 */
+    /* The per-layer arguments flashinfer_backend.py passes with every attention call
+     * (forward_extend / forward_decode: logits_soft_cap = layer.logit_cap, k_scale,
+     * v_scale); the pages do not define them further, the readings taken are:
+     *   logit_j = cap * tanh(sm_scale * k_scale * q.k_j / cap)   (cap > 0; <= 0: no cap)
+     *   out = v_scale * sum_j softmax_j v_j                      (K, V dequantised)
+     * A scale <= 0 means 1 (so a zero-initialised descriptor keeps the plain method).
+     * The caches stay bf16 here; the scales are plain multipliers. */
+    float logits_soft_cap;
+    float k_scale;
+    float v_scale;
 } pkv_plan_desc;
 
 typedef struct pkv_plan pkv_plan;

@@ -121,6 +121,9 @@ int validate(const pkv_plan_desc *d, std::vector<HostRequest> &reqs)
         return fail(PKV_ERR_INVALID_ARG, "sm_scale is not finite");
     if (!(d->sm_scale > 0.f))
         return fail(PKV_ERR_UNSUPPORTED, "sm_scale must be positive");
+    for (float x : {d->logits_soft_cap, d->k_scale, d->v_scale})
+        if (!(x == x) || std::isinf(x))
+            return fail(PKV_ERR_INVALID_ARG, "logits_soft_cap, k_scale and v_scale must be finite");
     if (d->kind != PKV_DECODE &&
         d->num_qo_heads / d->num_kv_heads > kPrefillRows)
         return fail(PKV_ERR_UNSUPPORTED, "query-head group %d exceeds %d",
@@ -688,6 +691,7 @@ int pkv_plan_update(pkv_plan *plan, const pkv_plan_desc *desc, void *stream_)
     if (d.kind != o.kind || d.num_qo_heads != o.num_qo_heads || d.num_kv_heads != o.num_kv_heads ||
         d.head_dim != o.head_dim || d.page_size != o.page_size || W != o.window_left ||
         (d.causal != 0) != (o.causal != 0) || d.sm_scale != o.sm_scale || d.dtype != o.dtype ||
+        d.logits_soft_cap != o.logits_soft_cap || d.k_scale != o.k_scale || d.v_scale != o.v_scale ||
         d.num_pages != o.num_pages || d.kv_indices != o.kv_indices)
         return fail(PKV_ERR_INVALID_ARG,
                     "update must keep kind, heads, head_dim, page_size, window_left, causal, sm_scale, "
@@ -850,7 +854,11 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
         p.page_size = d.page_size;
         p.page_shift = page_shift_of(d.page_size);
         p.num_pages = d.num_pages;
-        p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
+        const LogitFactors lf = logit_factors(d);
+        p.sm_scale_log2 = lf.sm_scale_log2;
+        p.cap_in = lf.cap_in;
+        p.cap_out = lf.cap_out;
+        p.v_scale = lf.v_scale;
         if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
             return cuda_fail(ce, "cudaEventRecord");
         ce = launch_decode(p, d.head_dim, plan->capturable ? (int)plan->cap_items : plan->num_items, stream,
@@ -881,7 +889,11 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.page_shift = page_shift_of(d.page_size);
     p.num_pages = d.num_pages;
     p.window_left = d.window_left;
-    p.sm_scale_log2 = d.sm_scale * 1.4426950408889634f;
+    const LogitFactors lf = logit_factors(d);
+    p.sm_scale_log2 = lf.sm_scale_log2;
+    p.cap_in = lf.cap_in;
+    p.cap_out = lf.cap_out;
+    p.v_scale = lf.v_scale;
     p.ragged = d.kind == PKV_PREFILL_RAGGED ? 1 : 0;
     p.total_kv = (int32_t)plan->total_kv;
     if (p.ragged) {

@@ -284,7 +284,10 @@ __global__ void __launch_bounds__(DecTraits<D, TT>::kThreads, DecTraits<D, TT>::
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int j = tok_base + nt * 8 + (e & 1);
-                    sc[nt][e] = (j >= it.j0 && j < it.j1) ? sc[nt][e] * scale : -INFINITY;
+                    float x = sc[nt][e];
+                    if (p.cap_in > 0.f)
+                        x = p.cap_out * soft_cap_tanh(x * p.cap_in);  // soft cap on the raw dot product
+                    sc[nt][e] = (j >= it.j0 && j < it.j1) ? x * scale : -INFINITY;
                 }
             float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
             float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
@@ -362,7 +365,8 @@ __global__ void __launch_bounds__(DecTraits<D, TT>::kThreads, DecTraits<D, TT>::
             for (int w = 0; w < NW; ++w)
                 L += red_l[w][tid] * fast_exp2(red_m[w][tid] - ref);
             row_m[tid] = M;
-            row_inv_l[tid] = L > 0.f ? 1.f / L : 0.f;
+            // partial states stay unscaled; v_scale goes on the final output
+            row_inv_l[tid] = L > 0.f ? (it.partial >= 0 ? 1.f : p.v_scale) / L : 0.f;
             if (tid < it.nheads && !abort_flag) {
                 const float lse_v = L > 0.f ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
                 const int h = it.head0 + tid;
@@ -466,7 +470,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT>::kThreads, DecTraits<D, TT>::
                             sum += wgt;
                         }
                     }
-                    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+                    const float inv = sum > 0.f ? p.v_scale / sum : 0.f;
                     uint16_t *dst = p.out + ((size_t)rq.qo_begin * p.num_qo_heads + h) * D + c0;
 #pragma unroll
                     for (int q8 = 0; q8 < CPT / 8; ++q8) {

@@ -97,7 +97,10 @@ struct DecodeParams {
     int32_t page_size;
     int32_t page_shift;  // log2(page_size) when a power of two, else -1
     int32_t num_pages;
-    float sm_scale_log2; // sm_scale * log2(e)
+    float sm_scale_log2; // sm_scale * k_scale * log2(e)
+    float cap_in;        // soft cap: dot -> cap_out * tanh(dot * cap_in); cap_in = 0: none
+    float cap_out;
+    float v_scale;       // multiplies the final output
 };
 
 struct MergePartialsParams {
@@ -108,6 +111,7 @@ struct MergePartialsParams {
     float *lse;
     int32_t num_items;
     int32_t num_qo_heads;
+    float v_scale;  // multiplies the merged output
 };
 
 struct PrefillParams {
@@ -130,10 +134,31 @@ struct PrefillParams {
     int32_t num_pages;
     int32_t window_left;
     int32_t total_q;         // rows of q (bound of the query tensor map)
-    float sm_scale_log2;
+    float sm_scale_log2;     // sm_scale * k_scale * log2(e)
+    float cap_in;            // soft cap, as in DecodeParams
+    float cap_out;
+    float v_scale;
     int32_t ragged;          // 1: K/V are contiguous [total_kv, H_kv, d], kv_page_begin = token offset
     int32_t total_kv;        // ragged: rows of K/V (bound of their tensor maps)
 };
+
+// The logit and output factors of a plan descriptor (k_scale folded into the logit
+// scale; scales <= 0 mean 1; a soft cap <= 0 means none).
+struct LogitFactors {
+    float sm_scale_log2, cap_in, cap_out, v_scale;
+};
+inline LogitFactors logit_factors(const pkv_plan_desc &d)
+{
+    const float ks = d.k_scale > 0.f ? d.k_scale : 1.f;
+    const float vs = d.v_scale > 0.f ? d.v_scale : 1.f;
+    const float s = d.sm_scale * ks;
+    LogitFactors f;
+    f.sm_scale_log2 = s * 1.4426950408889634f;
+    f.cap_in = d.logits_soft_cap > 0.f ? s / d.logits_soft_cap : 0.f;
+    f.cap_out = d.logits_soft_cap > 0.f ? d.logits_soft_cap / s : 0.f;
+    f.v_scale = vs;
+    return f;
+}
 
 // Launchers (one per kernel family); return cudaGetLastError() of the launch.
 // tile: KV tokens per stage, 64 or (head_dim <= 128) 32.

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(256) merge_partials_kernel(const MergePartials
             sum += w;
         }
     }
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    const float inv = sum > 0.f ? p.v_scale / sum : 0.f;
 #pragma unroll
     for (int i = 0; i < N; ++i)
         acc[i] *= inv;

@@ -86,6 +86,9 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
         return noalloc_fail(PKV_ERR_UNSUPPORTED, "head_dim not in {64, 128, 256}");
     if (d->page_size <= 0 || d->num_pages < 0 || d->dtype != PKV_BF16)
         return noalloc_fail(PKV_ERR_INVALID_ARG, "page_size, num_pages or dtype");
+    for (float x : {d->logits_soft_cap, d->k_scale, d->v_scale})
+        if (!(x == x) || std::isinf(x))
+            return noalloc_fail(PKV_ERR_INVALID_ARG, "logits_soft_cap, k_scale and v_scale must be finite");
     if (!(d->sm_scale > 0.f) || std::isinf(d->sm_scale))
         return noalloc_fail(PKV_ERR_UNSUPPORTED, "sm_scale must be positive and finite");
     if (d->kv_indptr[0] != 0)
@@ -218,7 +221,11 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
     p.page_size = d->page_size;
     p.page_shift = page_shift(d->page_size);
     p.num_pages = d->num_pages;
-    p.sm_scale_log2 = d->sm_scale * 1.4426950408889634f;
+    const LogitFactors lf = logit_factors(*d);
+    p.sm_scale_log2 = lf.sm_scale_log2;
+    p.cap_in = lf.cap_in;
+    p.cap_out = lf.cap_out;
+    p.v_scale = lf.v_scale;
     int64_t max_keys = 0;
     for (const DecodeItem &it : items)
         max_keys = std::max<int64_t>(max_keys, it.j1 - it.j0);
@@ -238,6 +245,7 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
         m.lse = lse;
         m.num_items = (int32_t)merges.size();
         m.num_qo_heads = d->num_qo_heads;
+        m.v_scale = p.v_scale;
         ce = launch_merge_partials(m, d->head_dim, stream);
         if (ce != cudaSuccess)
             return noalloc_fail(PKV_ERR_CUDA, std::string("merge launch: ") + cudaGetErrorString(ce));

@@ -198,6 +198,12 @@ __global__ void __launch_bounds__(384, 1)
                 for (int c = 0; c < T / 32; ++c)
                     tmem_ld32(tS + 32 * c, *reinterpret_cast<float(*)[32]>(&s[32 * c]));
                 tmem_wait_ld();
+                if (p.cap_in > 0.f) {
+                    // soft cap on the raw dot products, before the mask
+#pragma unroll
+                    for (int c = 0; c < T; ++c)
+                        s[c] = p.cap_out * soft_cap_tanh(s[c] * p.cap_in);
+                }
 
                 const int j0 = prefill_kv_key_at(it, j, T);
                 bool need_mask = j0 + T > rq.kv_len;
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(384, 1)
             const int h = it.kv_head * g + r % g;
             const size_t orow = (size_t)(rq.qo_begin + tok) * p.num_qo_heads + h;
             uint16_t *dst = p.out + orow * D;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? p.v_scale / l : 0.f;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];

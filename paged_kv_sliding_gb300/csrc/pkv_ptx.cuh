@@ -100,6 +100,16 @@ __device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1)
         : "f"(a0), "f"(a1));
 }
 
+// tanh from the exponential: tanh(y) = 1 - 2 / (2^(2 y log2 e) + 1), clamped to
+// |y| <= 15 (tanh(15) is 1 to fp32 precision). Absolute error ~1e-7.
+__device__ __forceinline__ float soft_cap_tanh(float y)
+{
+    y = fminf(fmaxf(y, -15.f), 15.f);
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(e) : "f"(y * 2.8853900817779268f));
+    return 1.f - __fdividef(2.f, e + 1.f);
+}
+
 __device__ __forceinline__ void record_status(int32_t *status, int32_t code)
 {
     atomicCAS(status, 0, code);

@@ -65,6 +65,9 @@ class PlanDesc(ctypes.Structure):
         ("fixed_split_size", ctypes.c_int32),
         ("disable_split_kv", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
+        ("logits_soft_cap", ctypes.c_float),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
     ]
 
 
@@ -176,7 +179,8 @@ class Plan:
                  page_size: int = 1, num_pages: int = 0, window_left: int = -1, causal: bool = True,
                  sm_scale: Optional[float] = None, qo_indptr=None, q_start=None,
                  fixed_split_size: int = -1, disable_split_kv: bool = False, stream=None,
-                 capacity: Optional[dict] = None):
+                 capacity: Optional[dict] = None, logits_soft_cap: float = 0.0, k_scale: float = 1.0,
+                 v_scale: float = 1.0):
         """kind: "prefill", "decode" or "prefill_ragged" (K/V passed to run() are
         contiguous [total_kv, H_kv, d]; kv_indptr counts tokens; no page table).
         capacity={"max_batch": B, "max_total_q": Q}: a capturable plan (its run may
@@ -219,6 +223,9 @@ class Plan:
         d.fixed_split_size = int(fixed_split_size)
         d.disable_split_kv = 1 if disable_split_kv else 0
         d.dtype = PKV_BF16
+        d.logits_soft_cap = float(logits_soft_cap)
+        d.k_scale = float(k_scale)
+        d.v_scale = float(v_scale)
         self._desc = d
         if capacity is None:
             _check(self._lib.pkv_plan_create(ctypes.byref(self._handle), ctypes.byref(d),

@@ -36,7 +36,7 @@ def test_header_declares_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_entry_points():
         assert hasattr(lib, name), name
-    assert lib.pkv_abi_version() == 2
+    assert lib.pkv_abi_version() == 3
 
 
 def test_status_strings(lib):

@@ -365,3 +365,31 @@ def test_plan_info(pkv):
     assert info["mask_mode"] == 1
     wp = wl.tiny_extend()
     assert pkv.plan_for(wp.to("cuda")).info["mask_mode"] == 2
+
+
+# ---------------------------------------------------- logits soft cap and K/V scales
+
+CAP_SCALES = dict(logits_soft_cap=4.0, k_scale=1.5, v_scale=0.75)
+
+
+@pytest.mark.parametrize("d,P", [(64, 16), (128, 1), (128, 16), (256, 16)])
+def test_prefill_soft_cap_and_scales(pkv, oracle_lib, d, P):
+    w = wl.make_workload(name="cap", qo_lens=[70, 1, 300, 129], kv_lens=[70, 200, 333, 700], num_qo_heads=8,
+                         num_kv_heads=2, head_dim=d, page_size=P, window_left=100, causal=True, seed=d + P)
+    out, lse, _ = gpu_run(pkv, w, **CAP_SCALES)
+    ref_out, ref_lse = run_oracle(oracle_lib, w, **CAP_SCALES)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"soft cap prefill d={d} P={P}")
+
+
+@pytest.mark.parametrize("W,split", [(127, -1), (-1, -1), (-1, 64)])
+def test_decode_soft_cap_and_scales(pkv, oracle_lib, W, split):
+    rng = np.random.default_rng(abs(W) + abs(split) + 7)
+    kv = rng.integers(1, 2000, size=20).tolist()
+    w = wl.make_workload(name="capd", kind="decode", qo_lens=np.ones(len(kv)), kv_lens=kv, num_qo_heads=32,
+                         num_kv_heads=8, head_dim=128, page_size=16, window_left=W, causal=True, seed=5,
+                         layout_rng=rng)
+    out, lse, info = gpu_run(pkv, w, fixed_split_size=split, **CAP_SCALES)
+    if split == 64:
+        assert info["num_partials"] > 0
+    ref_out, ref_lse = run_oracle(oracle_lib, w, **CAP_SCALES)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"soft cap decode W={W} split={split}")

@@ -87,6 +87,26 @@ def test_noalloc_matches_plan_run_twice(pkv, W, split):
         assert r["bad_out"] == 0 and r["bad_lse"] == 0, (call, r)
 
 
+def test_noalloc_soft_cap_and_scales_match_the_oracle(pkv, oracle_lib):
+    """Split so that the separate merge kernel applies v_scale."""
+    from tests.helpers import assert_parity, run_oracle
+    w = wl.batch_decode(-1, device="cuda", batch=12)
+    kv_indices = torch.as_tensor(w.kv_indices, dtype=torch.int32, device="cuda")
+    d, keep = _desc(pkv, w, kv_indices, fixed_split_size=256)
+    d.logits_soft_cap, d.k_scale, d.v_scale = 4.0, 1.5, 0.75
+    lib = pkv.load_library()
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.q.shape[:2], dtype=torch.float32, device="cuda")
+    rc = lib.pkv_decode_noalloc(ctypes.byref(d), ctypes.c_void_p(w.q.data_ptr()),
+                                ctypes.c_void_p(w.k_cache.data_ptr()), ctypes.c_void_p(w.v_cache.data_ptr()),
+                                ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == pkv.PKV_OK, lib.pkv_last_error()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = run_oracle(oracle_lib, w, logits_soft_cap=4.0, k_scale=1.5, v_scale=0.75)
+    assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, what="noalloc soft cap")
+
+
 def test_noalloc_rejects_oversize_batch(pkv):
     """A batch whose partial states exceed the fixed scratch is refused on the host
     with a message naming the size, before any launch."""
