@@ -109,6 +109,9 @@ __global__ void __launch_bounds__(DecTraits<D, TT>::kThreads, DecTraits<D, TT>::
         fence_proxy_async_smem();
     }
     __syncthreads();
+    // Everything above reads only the plan's own data; q, the caches and the page
+    // table may come from the previous kernel in the stream.
+    grid_dependency_wait();
 
     if (warp == Tr::kCompute) {
         // ------------------------------------------------------------ producer
@@ -341,6 +344,8 @@ __global__ void __launch_bounds__(DecTraits<D, TT>::kThreads, DecTraits<D, TT>::
             abort_flag = 1;
         }
 
+        // This CTA's loads are done: the next grid may start its set-up.
+        grid_launch_dependents();
         // Merge the compute warps' states (named barrier 1 over the compute threads).
         l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
         l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
@@ -530,8 +535,20 @@ cudaError_t launch_decode_dt(const DecodeParams &p, const CUtensorMap &tk, const
             return e;
         configured = true;
     }
-    decode_kernel<D, TMA_KV, TT><<<num_items, Tr::kThreads, Tr::kDynSmem, s>>>(p, tk, tv);
-    return cudaGetLastError();
+    // Programmatic stream serialisation: this grid's set-up (barriers, work item)
+    // may overlap the tail of the previous kernel in the stream; the kernel waits
+    // for that kernel's completion before it touches q, the caches or the page table.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)num_items);
+    cfg.blockDim = dim3(Tr::kThreads);
+    cfg.dynamicSmemBytes = Tr::kDynSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, TMA_KV, TT>, p, tk, tv);
 }
 
 }  // namespace

@@ -110,6 +110,12 @@ __device__ __forceinline__ float soft_cap_tanh(float y)
     return 1.f - __fdividef(2.f, e + 1.f);
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their writes are visible (a no-op for an ordinary launch), and let
+// the next grid in the stream start its own set-up.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 __device__ __forceinline__ void record_status(int32_t *status, int32_t code)
 {
     atomicCAS(status, 0, code);
