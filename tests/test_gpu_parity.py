@@ -225,7 +225,7 @@ def test_batch_decode_full(pkv, oracle_lib, W):
 
 @pytest.mark.parametrize("P,d", [(16, 128), (4, 128), (16, 256), (1, 64)])
 def test_decode_many_short_items(pkv, oracle_lib, P, d):
-    """Short windows over many requests: several work items per CTA in one round."""
+    """Short windows over many requests: 1200 work items in one launch (32-token tiles)."""
     rng = np.random.default_rng(P * d)
     kv = rng.integers(1, 300, size=300).tolist()
     w = wl.make_workload(name="short", kind="decode", qo_lens=np.ones(len(kv)), kv_lens=kv,
