@@ -62,6 +62,13 @@ def _load():
             lib.pkv_oracle_attention_ext.argtypes = [
                 i64, p, p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double, p, p, p, p, i64, p, p]
+            lib.pkv_oracle_attention_kv.restype = ctypes.c_int
+            lib.pkv_oracle_attention_kv.argtypes = [
+                i64, p, p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double, p, ctypes.c_int,
+                p, p, p, i64, p, p]
+            lib.pkv_oracle_decode_fp8.restype = ctypes.c_int
+            lib.pkv_oracle_decode_fp8.argtypes = [ctypes.c_int, p, i64, p]
             lib.pkv_oracle_set_threads.restype = ctypes.c_int
             lib.pkv_oracle_set_threads.argtypes = [ctypes.c_int]
             lib.pkv_oracle_merge_state.restype = ctypes.c_int
@@ -86,6 +93,35 @@ def _bf16_bits(t):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+KV_DTYPES = {"bf16": 0, "e4m3": 2, "e5m2": 3}
+
+
+def _cache_bytes(t):
+    """A CPU cache tensor -> (kv_dtype code, contiguous ndarray of its raw elements).
+
+    bf16 tensors (or uint16 arrays of bf16 bits) give code 0; float8_e4m3fn and
+    float8_e5m2 tensors give codes 2 and 3 with their bytes."""
+    if isinstance(t, np.ndarray):
+        return 0, _bf16_bits(t)
+    import torch
+    if t.dtype == torch.float8_e4m3fn:
+        return 2, t.contiguous().view(torch.uint8).numpy()
+    if t.dtype == torch.float8_e5m2:
+        return 3, t.contiguous().view(torch.uint8).numpy()
+    return 0, _bf16_bits(t)
+
+
+def decode_fp8(codes, fmt: str):
+    """Values of 8-bit codes (uint8 array) in format "e4m3" or "e5m2", as float64."""
+    lib = _load()
+    codes = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(codes.shape, dtype=np.float64)
+    rc = lib.pkv_oracle_decode_fp8(KV_DTYPES[fmt], _ptr(codes), codes.size, _ptr(out))
+    if rc != OK:
+        raise ValueError(f"unknown 8-bit format {fmt!r}")
+    return out
+
+
 def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
@@ -101,9 +137,10 @@ def attention(*, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, num_qo_head
               v_scale=1.0):
     """Reference attention in float64.
 
-    q: bf16 [total_q, H_qo, d]; k_cache, v_cache: bf16 [num_pages, P, H_kv, d]
-    (CPU torch tensors or uint16 arrays of bf16 bits). Returns (out, lse) as float64
-    arrays [n, H_qo, d] and [n, H_qo], n = total_q, or len(rows) for a row subset.
+    q: bf16 [total_q, H_qo, d]; k_cache, v_cache: [num_pages, P, H_kv, d] CPU torch
+    tensors of bf16, float8_e4m3fn or float8_e5m2 (both the same), or uint16 arrays of
+    bf16 bits. Returns (out, lse) as float64 arrays [n, H_qo, d] and [n, H_qo],
+    n = total_q, or len(rows) for a row subset.
     """
     lib = _load()
     qo_indptr = _i32(qo_indptr)
@@ -114,8 +151,10 @@ def attention(*, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, num_qo_head
     batch = len(kv_last_page_len)
     assert len(qo_indptr) == batch + 1 and len(kv_indptr) == batch + 1
     qb = _bf16_bits(q)
-    kb = _bf16_bits(k_cache)
-    vb = _bf16_bits(v_cache)
+    kv_dtype, kb = _cache_bytes(k_cache)
+    vdt, vb = _cache_bytes(v_cache)
+    if vdt != kv_dtype:
+        raise ValueError("k_cache and v_cache must have the same element type")
     if num_pages is None:
         num_pages = kb.shape[0]
     total_q = int(qo_indptr[-1]) if batch > 0 else 0
@@ -127,11 +166,11 @@ def attention(*, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, num_qo_head
         n = total_q
     out = np.zeros((n, num_qo_heads, head_dim), dtype=np.float64)
     lse = np.zeros((n, num_qo_heads), dtype=np.float64)
-    rc = lib.pkv_oracle_attention_ext(
+    rc = lib.pkv_oracle_attention_kv(
         batch, _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len),
         _ptr(q_start), num_qo_heads, num_kv_heads, head_dim, page_size, int(num_pages),
         int(window_left), int(bool(causal)), float(sm_scale), float(logits_soft_cap), float(k_scale),
-        float(v_scale), _ptr(qb), _ptr(kb), _ptr(vb),
+        float(v_scale), _ptr(qb), kv_dtype, _ptr(kb), _ptr(vb),
         _ptr(sel), 0 if sel is None else len(sel), _ptr(out), _ptr(lse))
     if rc != OK:
         raise ValueError(f"oracle rejected its input (status {rc})")

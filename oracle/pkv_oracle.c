@@ -53,6 +53,13 @@
  *
  * bf16 inputs are widened to double exactly (a bf16 value is the top half of an
  * IEEE binary32); all arithmetic is double.
+ *
+ * 8-bit caches (pkv_oracle_attention_kv): flashinfer_backend.py names
+ * torch.float8_e4m3fn and torch.float8_e5m2 as KV cache dtypes
+ * (should_use_tensor_core) and passes k_scale / v_scale with every call. Each
+ * byte is decoded to its exact value from the format's definition (the OCP 8-bit
+ * floating point formats E4M3 and E5M2, below) and the attention above runs on
+ * those values, k_scale and v_scale dequantising as stated.
  */
 #include <math.h>
 #include <omp.h>
@@ -70,6 +77,62 @@ static double bf16_bits_to_double(uint16_t bits)
     float f;
     memcpy(&f, &word, sizeof f);
     return (double)f;
+}
+
+/*
+ * E4M3: sign bit, 4 exponent bits with bias 7, 3 mantissa bits. Exponent field 0
+ * holds zero and the subnormals (m/8) * 2^-6; S.1111.111 is NaN; there are no
+ * infinities, so the largest finite value is 1.75 * 2^8 = 448.
+ */
+static double e4m3_to_double(uint8_t x)
+{
+    const int sign = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * E5M2: sign bit, 5 exponent bits with bias 15, 2 mantissa bits (IEEE-like).
+ * Exponent field 0 holds zero and the subnormals (m/4) * 2^-14; field 31 is
+ * infinity (m = 0) or NaN.
+ */
+static double e5m2_to_double(uint8_t x)
+{
+    const int sign = x >> 7, e = (x >> 2) & 31, m = x & 3;
+    double v;
+    if (e == 31)
+        v = m == 0 ? INFINITY : NAN;
+    else if (e == 0)
+        v = ldexp((double)m / 4.0, -14);
+    else
+        v = ldexp(1.0 + (double)m / 4.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* Element idx of a cache of kv_dtype 0 (bf16), 2 (E4M3) or 3 (E5M2). */
+static double cache_elem(const void *cache, int64_t idx, int kv_dtype)
+{
+    if (kv_dtype == 2)
+        return e4m3_to_double(((const uint8_t *)cache)[idx]);
+    if (kv_dtype == 3)
+        return e5m2_to_double(((const uint8_t *)cache)[idx]);
+    return bf16_bits_to_double(((const uint16_t *)cache)[idx]);
+}
+
+/* Exposed for the pins: decode n 8-bit codes of format kv_dtype (2 or 3). */
+int pkv_oracle_decode_fp8(int kv_dtype, const uint8_t *codes, int64_t n, double *out)
+{
+    if (kv_dtype != 2 && kv_dtype != 3)
+        return PKV_ORACLE_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kv_dtype == 2 ? e4m3_to_double(codes[i]) : e5m2_to_double(codes[i]);
+    return PKV_ORACLE_OK;
 }
 
 /* Threads used by the OpenMP loop below; returns the count now in force. */
@@ -118,7 +181,8 @@ static int64_t request_of_row(const int32_t *qo_indptr, int64_t batch, int64_t r
  *   rows == NULL: every row 0..qo_indptr[batch)-1, output row r at index r.
  *   rows != NULL: output row k holds global query row rows[k].
  * out: [n_out_rows, H_qo, d] double; lse: [n_out_rows, H_qo] double (may be NULL).
- * q: bf16 bits [total_q, H_qo, d]; caches: bf16 bits [num_pages, P, H_kv, d].
+ * q: bf16 bits [total_q, H_qo, d]; caches [num_pages, P, H_kv, d]: bf16 bits
+ * (kv_dtype 0) or E4M3 / E5M2 bytes (kv_dtype 2 / 3).
  * Returns 0, PKV_ORACLE_BAD_ARG, or PKV_ORACLE_BAD_PAGE (a page id outside
  * [0, num_pages) met on a visible key).
  */
@@ -129,17 +193,19 @@ static double logit_of(double dot, double scale, double cap)
     return cap > 0.0 ? cap * tanh(s / cap) : s;
 }
 
-int pkv_oracle_attention_ext(int64_t batch, const int32_t *qo_indptr, const int32_t *kv_indptr,
-                             const int32_t *kv_indices, const int32_t *kv_last_page_len,
-                             const int32_t *q_start, int64_t num_qo_heads, int64_t num_kv_heads,
-                             int64_t head_dim, int64_t page_size, int64_t num_pages,
-                             int64_t window_left, int causal, double sm_scale, double soft_cap,
-                             double k_scale, double v_scale, const uint16_t *q,
-                             const uint16_t *k_cache, const uint16_t *v_cache, const int64_t *rows,
-                             int64_t n_rows, double *out, double *lse)
+int pkv_oracle_attention_kv(int64_t batch, const int32_t *qo_indptr, const int32_t *kv_indptr,
+                            const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                            const int32_t *q_start, int64_t num_qo_heads, int64_t num_kv_heads,
+                            int64_t head_dim, int64_t page_size, int64_t num_pages,
+                            int64_t window_left, int causal, double sm_scale, double soft_cap,
+                            double k_scale, double v_scale, const uint16_t *q, int kv_dtype,
+                            const void *k_cache, const void *v_cache, const int64_t *rows,
+                            int64_t n_rows, double *out, double *lse)
 {
     const double scale = sm_scale * k_scale;
     if (batch < 0 || num_kv_heads <= 0 || num_qo_heads <= 0 || head_dim <= 0 || page_size <= 0)
+        return PKV_ORACLE_BAD_ARG;
+    if (kv_dtype != 0 && kv_dtype != 2 && kv_dtype != 3)
         return PKV_ORACLE_BAD_ARG;
     if (num_qo_heads % num_kv_heads != 0)
         return PKV_ORACLE_BAD_ARG;
@@ -183,11 +249,10 @@ int pkv_oracle_attention_ext(int64_t batch, const int32_t *qo_indptr, const int3
                 bad = 1;
                 break;
             }
-            const uint16_t *krow =
-                k_cache + ((page * page_size + j % page_size) * num_kv_heads + hk) * head_dim;
+            const int64_t krow = ((page * page_size + j % page_size) * num_kv_heads + hk) * head_dim;
             double dot = 0.0;
             for (int64_t c = 0; c < head_dim; ++c)
-                dot += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
+                dot += bf16_bits_to_double(qrow[c]) * cache_elem(k_cache, krow + c, kv_dtype);
             const double s = logit_of(dot, scale, soft_cap);
             if (s > m)
                 m = s;
@@ -208,16 +273,15 @@ int pkv_oracle_attention_ext(int64_t batch, const int32_t *qo_indptr, const int3
                 continue;
             int64_t page = kv_indices[(int64_t)kv_indptr[b] + j / page_size];
             int64_t slot = (page * page_size + j % page_size) * num_kv_heads + hk;
-            const uint16_t *krow = k_cache + slot * head_dim;
-            const uint16_t *vrow = v_cache + slot * head_dim;
+            const int64_t row0 = slot * head_dim;
             double dot = 0.0;
             for (int64_t c = 0; c < head_dim; ++c)
-                dot += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
+                dot += bf16_bits_to_double(qrow[c]) * cache_elem(k_cache, row0 + c, kv_dtype);
             const double s = logit_of(dot, scale, soft_cap);
             double w = exp(s - m);
             denom += w;
             for (int64_t c = 0; c < head_dim; ++c)
-                o[c] += w * bf16_bits_to_double(vrow[c]);
+                o[c] += w * cache_elem(v_cache, row0 + c, kv_dtype);
         }
         for (int64_t c = 0; c < head_dim; ++c)
             o[c] = v_scale * o[c] / denom;
@@ -225,6 +289,21 @@ int pkv_oracle_attention_ext(int64_t batch, const int32_t *qo_indptr, const int3
             lse[k_out * num_qo_heads + h] = m + log(denom);
     }
     return status;
+}
+
+int pkv_oracle_attention_ext(int64_t batch, const int32_t *qo_indptr, const int32_t *kv_indptr,
+                             const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                             const int32_t *q_start, int64_t num_qo_heads, int64_t num_kv_heads,
+                             int64_t head_dim, int64_t page_size, int64_t num_pages,
+                             int64_t window_left, int causal, double sm_scale, double soft_cap,
+                             double k_scale, double v_scale, const uint16_t *q,
+                             const uint16_t *k_cache, const uint16_t *v_cache, const int64_t *rows,
+                             int64_t n_rows, double *out, double *lse)
+{
+    return pkv_oracle_attention_kv(batch, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, q_start,
+                                   num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, window_left,
+                                   causal, sm_scale, soft_cap, k_scale, v_scale, q, 0, k_cache, v_cache,
+                                   rows, n_rows, out, lse);
 }
 
 int pkv_oracle_attention(int64_t batch, const int32_t *qo_indptr, const int32_t *kv_indptr,

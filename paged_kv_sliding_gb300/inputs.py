@@ -40,8 +40,8 @@ class Workload:
     causal: bool
     sm_scale: float
     q: torch.Tensor                # bf16 [total_q, H_qo, d]
-    k_cache: torch.Tensor          # bf16 [num_pages, P, H_kv, d]
-    v_cache: torch.Tensor          # bf16 [num_pages, P, H_kv, d]
+    k_cache: torch.Tensor          # bf16 (or an 8-bit float, see to_kv8) [num_pages, P, H_kv, d]
+    v_cache: torch.Tensor          # same type and shape as k_cache
     q_start: Optional[np.ndarray] = None  # int32 [B] or None
     meta: dict = field(default_factory=dict)
 
@@ -65,6 +65,20 @@ class Workload:
     def to(self, device) -> "Workload":
         return replace(self, q=self.q.to(device), k_cache=self.k_cache.to(device),
                        v_cache=self.v_cache.to(device))
+
+
+KV8_DTYPES = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
+
+def to_kv8(w: Workload, fmt: str, scale: float = 1.0) -> Workload:
+    """The workload with its K/V pages rounded to an 8-bit format ("e4m3" or "e5m2"),
+    as an 8-bit KV cache would hold them: each value is divided by `scale` (the
+    k_scale / v_scale a caller then passes) and cast with torch's round-to-nearest
+    conversion. q stays bf16."""
+    dt = KV8_DTYPES[fmt]
+    k = (w.k_cache.float() / scale).to(dt)
+    v = (w.v_cache.float() / scale).to(dt)
+    return replace(w, k_cache=k, v_cache=v, meta=dict(w.meta, kv_dtype=fmt))
 
 
 def paged_layout(kv_lens, page_size: int, rng: np.random.Generator,

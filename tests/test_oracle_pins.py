@@ -484,3 +484,44 @@ def test_kv_scales_equal_scaled_caches(oracle_lib):
                    logits_soft_cap=3.0)
     np.testing.assert_allclose(a[0], b[0], atol=1e-14)
     np.testing.assert_allclose(a[1], b[1], atol=1e-14)
+
+
+# ------------------------------------------------- 8-bit KV caches (oracle only)
+
+@pytest.mark.parametrize("fmt,dt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_fp8_codes_match_torch(oracle_lib, fmt, dt):
+    """Every one of the 256 codes decodes to torch's value of that code (NaN where
+    torch gives NaN)."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle_lib.decode_fp8(codes, fmt)
+    ref = torch.from_numpy(codes).view(dt).to(torch.float64).numpy()
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all(), codes[~same]
+
+
+def test_fp8_closed_forms(oracle_lib):
+    """Values fixed by the formats' definitions: largest finite values, smallest
+    subnormals, one, negative zero, and E5M2's infinity."""
+    e4 = oracle_lib.decode_fp8(np.array([0x7E, 0x01, 0x38, 0x80, 0xB8, 0x08, 0x7F], np.uint8), "e4m3")
+    assert list(e4[:6]) == [448.0, 2.0 ** -9, 1.0, 0.0, -1.0, 2.0 ** -6] and np.isnan(e4[6])
+    assert math.copysign(1.0, e4[3]) == -1.0
+    e5 = oracle_lib.decode_fp8(np.array([0x7B, 0x01, 0x3C, 0x7C, 0xFC, 0x04], np.uint8), "e5m2")
+    assert list(e5) == [57344.0, 2.0 ** -16, 1.0, math.inf, -math.inf, 2.0 ** -14]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_cache_equals_bf16_cache_of_its_values(oracle_lib, fmt):
+    """Every E4M3 and E5M2 value is exactly a bf16 value, so attention over an
+    8-bit cache must equal, bit for bit, attention over the bf16 cache that torch's
+    conversion makes of it (windows, soft cap and scales included)."""
+    from paged_kv_sliding_gb300.inputs import to_kv8
+    w = to_kv8(make_workload(name="kv8", qo_lens=[5, 1, 9], kv_lens=[40, 17, 9], num_qo_heads=4,
+                             num_kv_heads=2, head_dim=32, page_size=4, window_left=11, seed=77), fmt, 0.25)
+    kw = dict(k_scale=0.25, v_scale=0.25, logits_soft_cap=5.0)
+    a = run_oracle(oracle_lib, w, **kw)
+    b = run_oracle(oracle_lib, w, k_cache=w.k_cache.to(torch.bfloat16), v_cache=w.v_cache.to(torch.bfloat16), **kw)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # and the cache is not trivially bf16-like: rounding to 8 bits changed the values
+    assert not torch.equal(w.k_cache.to(torch.float32) * 0.25, make_workload(
+        name="kv8", qo_lens=[5, 1, 9], kv_lens=[40, 17, 9], num_qo_heads=4, num_kv_heads=2, head_dim=32,
+        page_size=4, window_left=11, seed=77).k_cache.float())
