@@ -384,7 +384,8 @@ def run_ours(args, rank, world):
     return line
 
 
-EXTRA = ("swa_prefill_p1", "swa_prefill_p16", "extend_prefix", "extend_ragged", "long_decode")
+EXTRA = ("swa_prefill_p1", "swa_prefill_p16", "extend_prefix", "extend_ragged", "long_decode",
+         "batch_decode_fp8", "long_decode_fp8")
 
 
 def bench_prefill_ragged(pkv, w, steps, warmup, flush):
@@ -445,6 +446,35 @@ def extra_workloads(pkv, args, peaks, flush, only=None):
         res[f"long_decode_256x32768_W{W}"] = {
             "gbs": bytes_per[0] / (k * 1e-3) / 1e9, "kernel_ms": k,
             "step_ms": statistics.mean(step_ms), "kv_gb": bytes_per[0] / 1e9,
+            "frac_hbm": bytes_per[0] / (k * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "splits": plans[0].info["num_partials"], "ctas": plans[0].info["num_work_items"]}
+        del w, plans, runs
+        torch.cuda.empty_cache()
+    # 8-bit KV caches (E4M3): the batch-decode windows and the long decode. GB/s counts
+    # the bytes of the 8-bit cache a pass must read (half of bf16's per key).
+    if want("batch_decode_fp8"):
+        w = wl.to_kv8(wl.batch_decode(device="cuda"), "e4m3")
+        plans, runs, bytes_per, step_ms, kern_ms, _ = bench_decode_windows(
+            pkv, w, wl.BATCH_DECODE_WINDOWS, steps, 3, flush)
+        for i, W in enumerate(wl.BATCH_DECODE_WINDOWS):
+            k = kern_ms[i] / steps
+            res[f"batch_decode_e4m3_W{W}"] = {
+                "gbs": bytes_per[i] / (k * 1e-3) / 1e9, "kernel_us": k * 1e3, "kv_mb": bytes_per[i] / 1e6,
+                "frac_hbm": bytes_per[i] / (k * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "keys_per_s": bytes_per[i] / (2 * w.num_kv_heads * w.head_dim) / (k * 1e-3),
+                "kv_tile": plans[i].info["kv_tile"], "ctas": plans[i].info["num_work_items"]}
+        res["batch_decode_e4m3_step_ms"] = statistics.mean(step_ms)
+        del w, plans, runs
+        torch.cuda.empty_cache()
+    if want("long_decode_fp8"):
+        base = wl.long_decode(-1, device="cuda")
+        w = wl.to_kv8(base, "e4m3")
+        del base
+        torch.cuda.empty_cache()
+        plans, runs, bytes_per, step_ms, kern_ms, _ = bench_decode_windows(pkv, w, [-1], steps, 2, flush)
+        k = kern_ms[0] / steps
+        res["long_decode_256x32768_W-1_e4m3"] = {
+            "gbs": bytes_per[0] / (k * 1e-3) / 1e9, "kernel_ms": k, "kv_gb": bytes_per[0] / 1e9,
             "frac_hbm": bytes_per[0] / (k * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "splits": plans[0].info["num_partials"], "ctas": plans[0].info["num_work_items"]}
         del w, plans, runs

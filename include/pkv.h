@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 3
+#define PKV_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define PKV_API __attribute__((visibility("default")))
@@ -87,7 +87,10 @@ typedef enum pkv_kind {
 
 typedef enum pkv_dtype {
     PKV_BF16 = 0,
-    PKV_F32 = 1 /* merge_state values only */
+    PKV_F32 = 1,     /* merge_state values only */
+    PKV_FP8_E4M3 = 2, /* 8-bit K/V caches (pkv_plan_desc.kv_dtype, DECODE plans): OCP E4M3,
+                         torch.float8_e4m3fn */
+    PKV_FP8_E5M2 = 3  /* OCP E5M2, torch.float8_e5m2 */
 } pkv_dtype;
 
 /*
@@ -126,11 +129,17 @@ typedef struct pkv_plan_desc {
      * v_scale); the pages do not define them further, the readings taken are:
      *   logit_j = cap * tanh(sm_scale * k_scale * q.k_j / cap)   (cap > 0; <= 0: no cap)
      *   out = v_scale * sum_j softmax_j v_j                      (K, V dequantised)
-     * A scale <= 0 means 1 (so a zero-initialised descriptor keeps the plain method).
-     * The caches stay bf16 here; the scales are plain multipliers. */
+     * A scale <= 0 means 1 (so a zero-initialised descriptor keeps the plain method). */
     float logits_soft_cap;
     float k_scale;
     float v_scale;
+    /* Element type of k_cache and v_cache: PKV_BF16 (0), or for DECODE plans an 8-bit
+     * float, PKV_FP8_E4M3 or PKV_FP8_E5M2 (flashinfer_backend.py, should_use_tensor_core,
+     * names torch.float8_e4m3fn and torch.float8_e5m2 as KV cache dtypes). The caches
+     * then hold one byte per element in the same [num_pages, page_size, H_kv, d]
+     * layout, K = k_scale * (stored value) and V = v_scale * (stored value); q and out
+     * stay bf16. PREFILL plans with an 8-bit cache return PKV_ERR_UNSUPPORTED. */
+    int32_t kv_dtype;
 } pkv_plan_desc;
 
 typedef struct pkv_plan pkv_plan;
@@ -193,7 +202,8 @@ PKV_API int pkv_plan_create_capturable(pkv_plan **out, const pkv_plan_desc *desc
  * pkv_plan_update: re-plan a capturable plan for a new batch, in place: host arrays
  * in `desc` (qo_indptr, kv_indptr, kv_last_page_len, q_start, batch_size,
  * fixed_split_size, disable_split_kv) may change; kind, head counts, head_dim,
- * page_size, window_left, causal, sm_scale, dtype, num_pages and the kv_indices
+ * page_size, window_left, causal, sm_scale, dtype, kv_dtype, logits_soft_cap, k_scale,
+ * v_scale, num_pages and the kv_indices
  * device pointer must equal the plan's (the caller rewrites that array's contents,
  * stream-ordered before the next run), else PKV_ERR_INVALID_ARG. A batch above the
  * capacity returns PKV_ERR_UNSUPPORTED and leaves the plan unchanged.

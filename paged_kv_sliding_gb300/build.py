@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
 
-SOURCES = ["pkv_api.cpp", "pkv_decode.cu", "pkv_merge.cu", "pkv_prefill.cu",
+SOURCES = ["pkv_api.cpp", "pkv_decode.cu", "pkv_decode_fp8.cu", "pkv_merge.cu", "pkv_prefill.cu",
            "pkv_noalloc.cu", "pkv_indices.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

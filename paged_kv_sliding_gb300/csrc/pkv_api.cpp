@@ -116,7 +116,12 @@ int validate(const pkv_plan_desc *d, std::vector<HostRequest> &reqs)
     if (d->num_pages < 0)
         return fail(PKV_ERR_INVALID_ARG, "num_pages %d < 0", d->num_pages);
     if (d->dtype != PKV_BF16)
-        return fail(PKV_ERR_UNSUPPORTED, "dtype %d: only PKV_BF16 q/kv/out are supported", d->dtype);
+        return fail(PKV_ERR_UNSUPPORTED, "dtype %d: only PKV_BF16 q/out are supported", d->dtype);
+    if (d->kv_dtype != PKV_BF16 && d->kv_dtype != PKV_FP8_E4M3 && d->kv_dtype != PKV_FP8_E5M2)
+        return fail(PKV_ERR_INVALID_ARG, "kv_dtype %d is not PKV_BF16, PKV_FP8_E4M3 or PKV_FP8_E5M2",
+                    d->kv_dtype);
+    if (d->kv_dtype != PKV_BF16 && d->kind != PKV_DECODE)
+        return fail(PKV_ERR_UNSUPPORTED, "8-bit K/V caches are supported by DECODE plans only");
     if (!(d->sm_scale == d->sm_scale) || std::isinf(d->sm_scale))
         return fail(PKV_ERR_INVALID_ARG, "sm_scale is not finite");
     if (!(d->sm_scale > 0.f))
@@ -692,10 +697,11 @@ int pkv_plan_update(pkv_plan *plan, const pkv_plan_desc *desc, void *stream_)
         d.head_dim != o.head_dim || d.page_size != o.page_size || W != o.window_left ||
         (d.causal != 0) != (o.causal != 0) || d.sm_scale != o.sm_scale || d.dtype != o.dtype ||
         d.logits_soft_cap != o.logits_soft_cap || d.k_scale != o.k_scale || d.v_scale != o.v_scale ||
+        d.kv_dtype != o.kv_dtype ||
         d.num_pages != o.num_pages || d.kv_indices != o.kv_indices)
         return fail(PKV_ERR_INVALID_ARG,
                     "update must keep kind, heads, head_dim, page_size, window_left, causal, sm_scale, "
-                    "dtype, num_pages and the kv_indices pointer of the plan");
+                    "dtype, kv_dtype, soft cap, scales, num_pages and the kv_indices pointer of the plan");
     if (d.batch_size > plan->cap_batch)
         return fail(PKV_ERR_UNSUPPORTED, "batch %d exceeds the plan's capacity %lld", d.batch_size,
                     (long long)plan->cap_batch);
@@ -859,6 +865,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
         p.cap_in = lf.cap_in;
         p.cap_out = lf.cap_out;
         p.v_scale = lf.v_scale;
+        p.kv_dtype = d.kv_dtype;
         if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
             return cuda_fail(ce, "cudaEventRecord");
         ce = launch_decode(p, d.head_dim, plan->capturable ? (int)plan->cap_items : plan->num_items, stream,

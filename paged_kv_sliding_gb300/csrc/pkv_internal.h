@@ -101,6 +101,7 @@ struct DecodeParams {
     float cap_in;        // soft cap: dot -> cap_out * tanh(dot * cap_in); cap_in = 0: none
     float cap_out;
     float v_scale;       // multiplies the final output
+    int32_t kv_dtype;    // element type of the caches (pkv_dtype: bf16 or an 8-bit float)
 };
 
 struct MergePartialsParams {
@@ -179,6 +180,13 @@ inline int decode_tile_for(int head_dim, int64_t max_keys, int64_t n_items, int 
 }
 // Page sizes whose pages the decode kernel loads with TMA boxes.
 bool decode_tma_page_size(int page_size);
+// 4-D tensor map [page, slot, KV head, d] over a cache of kv_dtype elements, boxes of
+// one 128-byte plane (64 bytes for 8-bit d 64) x box_rows slots.
+bool encode_kv_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_heads, int page_size,
+                   int num_pages, int box_rows, int kv_dtype);
+// The 8-bit-cache decode kernels (p.kv_dtype = PKV_FP8_E4M3 or PKV_FP8_E5M2).
+cudaError_t launch_decode_kv8(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile,
+                              bool tma, const CUtensorMap &tk, const CUtensorMap &tv);
 cudaError_t launch_merge_partials(const MergePartialsParams &p, int head_dim, cudaStream_t s);
 cudaError_t launch_merge_state(const void *v_a, const float *s_a, const void *v_b,
                                const float *s_b, void *v_out, float *s_out, int64_t rows,

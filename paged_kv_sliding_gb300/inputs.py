@@ -76,9 +76,16 @@ def to_kv8(w: Workload, fmt: str, scale: float = 1.0) -> Workload:
     k_scale / v_scale a caller then passes) and cast with torch's round-to-nearest
     conversion. q stays bf16."""
     dt = KV8_DTYPES[fmt]
-    k = (w.k_cache.float() / scale).to(dt)
-    v = (w.v_cache.float() / scale).to(dt)
-    return replace(w, k_cache=k, v_cache=v, meta=dict(w.meta, kv_dtype=fmt))
+
+    def cast(t):
+        out = torch.empty(t.shape, dtype=dt, device=t.device)
+        src, dst = t.view(-1), out.view(-1)
+        chunk = 1 << 28
+        for s in range(0, src.numel(), chunk):
+            dst[s:s + chunk] = (src[s:s + chunk].float() / scale).to(dt)
+        return out
+
+    return replace(w, k_cache=cast(w.k_cache), v_cache=cast(w.v_cache), meta=dict(w.meta, kv_dtype=fmt))
 
 
 def paged_layout(kv_lens, page_size: int, rng: np.random.Generator,

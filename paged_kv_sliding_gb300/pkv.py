@@ -31,6 +31,13 @@ PKV_DECODE = 1
 PKV_PREFILL_RAGGED = 2
 PKV_BF16 = 0
 PKV_F32 = 1
+PKV_FP8_E4M3 = 2
+PKV_FP8_E5M2 = 3
+
+# Element types of the K/V caches, by name and by torch dtype.
+KV_DTYPES = {"bf16": PKV_BF16, "e4m3": PKV_FP8_E4M3, "e5m2": PKV_FP8_E5M2}
+_KV_TORCH = {PKV_BF16: torch.bfloat16, PKV_FP8_E4M3: torch.float8_e4m3fn,
+             PKV_FP8_E5M2: torch.float8_e5m2}
 
 EXPORTED = ("pkv_plan_create", "pkv_run", "pkv_merge_state", "pkv_plan_destroy",
             "pkv_plan_get_info", "pkv_plan_device_status", "pkv_status_string",
@@ -68,6 +75,7 @@ class PlanDesc(ctypes.Structure):
         ("logits_soft_cap", ctypes.c_float),
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
+        ("kv_dtype", ctypes.c_int32),
     ]
 
 
@@ -180,14 +188,21 @@ class Plan:
                  sm_scale: Optional[float] = None, qo_indptr=None, q_start=None,
                  fixed_split_size: int = -1, disable_split_kv: bool = False, stream=None,
                  capacity: Optional[dict] = None, logits_soft_cap: float = 0.0, k_scale: float = 1.0,
-                 v_scale: float = 1.0):
+                 v_scale: float = 1.0, kv_dtype="bf16"):
         """kind: "prefill", "decode" or "prefill_ragged" (K/V passed to run() are
         contiguous [total_kv, H_kv, d]; kv_indptr counts tokens; no page table).
         capacity={"max_batch": B, "max_total_q": Q}: a capturable plan (its run may
-        be captured in a CUDA graph and replayed after update())."""
+        be captured in a CUDA graph and replayed after update()).
+        kv_dtype: element type of the caches, "bf16", "e4m3" or "e5m2" (or the torch
+        dtype); the 8-bit ones are for decode plans."""
         self._lib = load_library()
         self._handle = ctypes.c_void_p()
         self.kind = kind
+        if isinstance(kv_dtype, torch.dtype):
+            kv_dtype = {v: k for k, v in _KV_TORCH.items()}.get(kv_dtype, -1)
+        elif isinstance(kv_dtype, str):
+            kv_dtype = KV_DTYPES.get(kv_dtype, -1)
+        self._kv_torch = _KV_TORCH.get(int(kv_dtype))
         kv_indptr = _host_i32(kv_indptr)
         ragged = kind == "prefill_ragged"
         if kv_last_page_len is None:
@@ -226,6 +241,7 @@ class Plan:
         d.logits_soft_cap = float(logits_soft_cap)
         d.k_scale = float(k_scale)
         d.v_scale = float(v_scale)
+        d.kv_dtype = int(kv_dtype)
         self._desc = d
         if capacity is None:
             _check(self._lib.pkv_plan_create(ctypes.byref(self._handle), ctypes.byref(d),
@@ -270,9 +286,10 @@ class Plan:
             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
             return_lse: bool = False, stream=None):
         """Attention for the planned batch; returns out (and lse when asked)."""
-        for t, name in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
-            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-                raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor")
+        for t, name, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", self._kv_torch),
+                            (v_cache, "v_cache", self._kv_torch)):
+            if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
         if out is None:
             out = torch.empty_like(q)
         if return_lse and lse is None:
@@ -364,6 +381,6 @@ def plan_for(w, device="cuda", **over) -> Plan:
                 num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, page_size=w.page_size,
                 num_pages=w.num_pages, window_left=w.window_left, causal=w.causal,
                 sm_scale=w.sm_scale, qo_indptr=None if w.kind == "decode" else w.qo_indptr,
-                q_start=w.q_start)
+                q_start=w.q_start, kv_dtype=w.k_cache.dtype)
     args.update(over)
     return Plan(**args)

@@ -37,5 +37,6 @@ def attention_flops(w: Workload) -> int:
 
 
 def decode_kv_bytes(w: Workload) -> int:
-    """Bytes of K and V a decode pass must read: visible rows x 2 x H_kv x d x 2 B."""
-    return visible_pairs_per_head(w) * 2 * w.num_kv_heads * w.head_dim * 2
+    """Bytes of K and V a decode pass must read: visible rows x 2 x H_kv x d x the
+    cache's element size (2 B for bf16, 1 B for an 8-bit cache)."""
+    return visible_pairs_per_head(w) * 2 * w.num_kv_heads * w.head_dim * w.k_cache.element_size()

@@ -36,7 +36,7 @@ def test_header_declares_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_entry_points():
         assert hasattr(lib, name), name
-    assert lib.pkv_abi_version() == 3
+    assert lib.pkv_abi_version() == 4
 
 
 def test_status_strings(lib):
@@ -93,6 +93,10 @@ def _desc(**over):
     (dict(kv_last_page_len=np.array([5, 1], dtype=np.int32)), pkv.PKV_ERR_INVALID_ARG),
     (dict(kv_last_page_len=np.array([0, 1], dtype=np.int32)), pkv.PKV_ERR_INVALID_ARG),
     (dict(num_qo_heads=258, num_kv_heads=2), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(kv_dtype=1), pkv.PKV_ERR_INVALID_ARG),
+    (dict(kv_dtype=4), pkv.PKV_ERR_INVALID_ARG),
+    (dict(kv_dtype=pkv.PKV_FP8_E4M3), pkv.PKV_ERR_UNSUPPORTED),  # 8-bit caches: decode plans only
+    (dict(kv_dtype=pkv.PKV_FP8_E5M2, kind=pkv.PKV_PREFILL_RAGGED), pkv.PKV_ERR_UNSUPPORTED),
 ])
 def test_plan_rejects_bad_arguments(lib, over, status):
     d, keep = _desc(**over)
