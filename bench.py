@@ -346,7 +346,7 @@ def run_ours(args, rank, world):
                            "frac_hbm": b / (k / args.steps * 1e-3) / 1e9 / peaks["hbm_gbs"],
                            "splits": p.info["num_partials"], "ctas": p.info["num_work_items"]}
                   for W, b, k, p in zip(windows, bytes_per, kern_ms, plans)}
-    traffic = _profiled_traffic("decode", "batch_decode", "pkv_decode.cu")
+    traffic = _profiled_traffic("decode", "batch_decode", "pkv_decode_kernel.cuh")
 
     e2e_s, h2d, d2h = e2e_decode(pkv, w, windows, max(3, args.steps // 4), 2)
     e2e_s = _max_over_ranks(e2e_s, world)

@@ -28,7 +28,6 @@
 #pragma once
 
 #include <cfloat>
-#include <cuda_fp8.h>
 
 #include "pkv_internal.h"
 #include "pkv_sm100.cuh"
@@ -78,15 +77,34 @@ __device__ __forceinline__ uint32_t plane_off(int row, int c16)
 }
 
 // Four 8-bit values (a 32-bit word, lowest byte first) as two f16x2 words: {x0, x1}
-// and {x2, x3}. Every E4M3 and E5M2 value is exact in f16.
+// and {x2, x3}. Every E4M3 and E5M2 value is exact in f16; an E5M2 byte is the top
+// byte of its f16, so that format needs only byte moves.
 template <int KV>
 __device__ __forceinline__ void fp8x4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
-    constexpr __nv_fp8_interpretation_t kInterp = KV == PKV_FP8_E5M2 ? __NV_E5M2 : __NV_E4M3;
-    const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), kInterp);
-    const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), kInterp);
-    lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
-    hi = (uint32_t)b.x | ((uint32_t)b.y << 16);
+    if (KV == PKV_FP8_E5M2) {
+        lo = __byte_perm(w, 0u, 0x1404);
+        hi = __byte_perm(w, 0u, 0x3424);
+    } else {
+        asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
+            " cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+    }
+}
+
+// The same for a word of a transposed V load, whose bytes are (token 2c, column 2n),
+// (2c, 2n+1), (2c+1, 2n), (2c+1, 2n+1): even = f16x2 of column 2n for tokens 2c, 2c+1,
+// odd = the same for column 2n+1.
+template <int KV>
+__device__ __forceinline__ void fp8x4_pairs_to_f16x2(uint32_t w, uint32_t &even, uint32_t &odd)
+{
+    if (KV == PKV_FP8_E5M2) {
+        even = __byte_perm(w, 0u, 0x2404);
+        odd = __byte_perm(w, 0u, 0x3414);
+    } else {
+        fp8x4_to_f16x2<KV>(__byte_perm(w, 0u, 0x3120), even, odd);
+    }
 }
 
 template <int D, bool TMA_KV, int TT, int KV>
@@ -345,7 +363,10 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
                 __syncwarp();
             }
 
+            // Even and odd k-steps accumulate apart (sc, sc2) and are added at the end:
+            // half the length of the dependent MMA chain.
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             if (!KV8) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -354,8 +375,9 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
                     const int c16 = 2 * ks + (mi & 1);
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(kb + plane_off<TT>(row, c16), b0, b1, b2, b3);
-                    mma_bf16_16816(sc[0], qf[ks], b0, b1);
-                    mma_bf16_16816(sc[1], qf[ks], b2, b3);
+                    float (&acc)[2][4] = (ks & 1) ? sc2 : sc;
+                    mma_bf16_16816(acc[0], qf[ks], b0, b1);
+                    mma_bf16_16816(acc[1], qf[ks], b2, b3);
                 }
             } else {
                 // One 16-byte granule of an 8-bit K row = the 16 columns of one k-step.
@@ -371,21 +393,36 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
                     for (int m = 0; m < 4; ++m) {
                         uint32_t b0, b1;
                         fp8x4_to_f16x2<KV>(w[m], b0, b1);
-                        mma_f16_16816(sc[m & 1], qf[2 * kk + (m >> 1)], b0, b1);
+                        mma_f16_16816((m >> 1) ? sc2[m & 1] : sc[m & 1], qf[2 * kk + (m >> 1)], b0, b1);
                     }
                 }
             }
-            const int tok_base = wt0 + 2 * (lane & 3);
+            // log2-domain logits: the soft cap on the scaled dot product, or the plain
+            // scaled dot (a uniform branch); then the mask, on the edge tiles only.
+            if (p.cap_in > 0.f) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = tok_base + nt * 8 + (e & 1);
-                    // soft cap on the scaled dot product, or the plain scaled dot
-                    const float x = p.cap_in > 0.f ? cap_scale * soft_cap_tanh(sc[nt][e] * cap_in)
-                                                   : sc[nt][e] * scale;
-                    sc[nt][e] = (j >= it.j0 && j < it.j1) ? x : -INFINITY;
-                }
+                    for (int e = 0; e < 4; ++e)
+                        sc[nt][e] = cap_scale * soft_cap_tanh((sc[nt][e] + sc2[nt][e]) * cap_in);
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        sc[nt][e] = (sc[nt][e] + sc2[nt][e]) * scale;
+            }
+            if (partial) {
+                const int tok_base = wt0 + 2 * (lane & 3);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = tok_base + nt * 8 + (e & 1);
+                        if (j < it.j0 || j >= it.j1)
+                            sc[nt][e] = -INFINITY;
+                    }
+            }
             float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
             float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -408,12 +445,16 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
             }
             l[0] = l[0] * a0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
             l[1] = l[1] * a1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+            // O is rescaled only when a row maximum of the warp moved (a = 1 otherwise:
+            // skipping the multiply changes nothing).
+            if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                o[i][0] *= a0;
-                o[i][1] *= a0;
-                o[i][2] *= a1;
-                o[i][3] *= a1;
+                for (int i = 0; i < D / 8; ++i) {
+                    o[i][0] *= a0;
+                    o[i][1] *= a0;
+                    o[i][2] *= a1;
+                    o[i][3] *= a1;
+                }
             }
             if (!KV8) {
                 const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
@@ -445,8 +486,8 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {  // granule 2kk + h: words 2h (tokens 0-7), 2h+1 (8-15)
                         uint32_t e0, o0, e1, o1;
-                        fp8x4_to_f16x2<KV>(__byte_perm(w[2 * h], 0u, 0x3120), e0, o0);
-                        fp8x4_to_f16x2<KV>(__byte_perm(w[2 * h + 1], 0u, 0x3120), e1, o1);
+                        fp8x4_pairs_to_f16x2<KV>(w[2 * h], e0, o0);
+                        fp8x4_pairs_to_f16x2<KV>(w[2 * h + 1], e1, o1);
                         mma_f16_16816(o[4 * kk + 2 * h], pa, e0, e1);
                         mma_f16_16816(o[4 * kk + 2 * h + 1], pa, o0, o1);
                     }
