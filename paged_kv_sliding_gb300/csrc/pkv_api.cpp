@@ -774,7 +774,9 @@ int pkv_plan_get_info(const pkv_plan *plan, pkv_plan_info *info)
     info->workspace_bytes = (int64_t)plan->workspace_bytes;
     info->total_q = plan->total_q;
     info->kernels_per_run = (plan->num_items > 0 || plan->capturable) ? 1 : 0;
-    info->kv_tile = plan->desc.kind == PKV_DECODE ? plan->decode_tile : prefill_kv_tile(plan->desc.head_dim);
+    info->kv_tile = plan->desc.kind == PKV_DECODE
+                        ? decode_kernel_tile(plan->decode_tile, plan->desc.head_dim, plan->desc.kv_dtype)
+                        : prefill_kv_tile(plan->desc.head_dim);
     return PKV_OK;
 }
 

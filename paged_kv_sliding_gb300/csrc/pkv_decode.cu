@@ -35,22 +35,24 @@ bool encode_kv_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_he
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool decode_tma_page_size(int page_size)
+bool decode_tma_page_size(int page_size, int tile)
 {
+    // whole pages inside a stage, or whole stages inside a page
     if (page_size < 8 || page_size % 8 != 0)
         return false;
-    return page_size <= 64 ? 64 % page_size == 0 : page_size % 64 == 0;
+    return page_size <= tile ? tile % page_size == 0 : page_size % tile == 0;
 }
 
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile)
 {
     using dec::launch_decode_dt;
-    const bool tma = decode_tma_page_size(p.page_size);
     if (tile == 32 && head_dim > 128)
         return cudaErrorInvalidValue;
+    const int tt = decode_kernel_tile(tile, head_dim, p.kv_dtype);
+    const bool tma = decode_tma_page_size(p.page_size, tt);
     CUtensorMap tk{}, tv{};
     if (tma) {
-        const int rows = p.page_size < tile ? p.page_size : tile;
+        const int rows = p.page_size < tt ? p.page_size : tt;
         if (!encode_kv_map(&tk, p.k_cache, head_dim, p.num_kv_heads, p.page_size, p.num_pages, rows, p.kv_dtype) ||
             !encode_kv_map(&tv, p.v_cache, head_dim, p.num_kv_heads, p.page_size, p.num_pages, rows, p.kv_dtype))
             return cudaErrorInvalidValue;

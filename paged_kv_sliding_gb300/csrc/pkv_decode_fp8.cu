@@ -22,11 +22,13 @@ cudaError_t launch_kv(const DecodeParams &p, int head_dim, int num_items, cudaSt
         default: return cudaErrorInvalidValue;
         }
     }
+    // the long variant: 128-token stages, two 16-token sub-blocks per compute warp
+    // (decode_kernel_tile), except at head_dim 256
     switch (head_dim) {
-    case 64: return tma ? launch_decode_dt<64, true, 64, KV>(p, tk, tv, num_items, s)
-                        : launch_decode_dt<64, false, 64, KV>(p, tk, tv, num_items, s);
-    case 128: return tma ? launch_decode_dt<128, true, 64, KV>(p, tk, tv, num_items, s)
-                         : launch_decode_dt<128, false, 64, KV>(p, tk, tv, num_items, s);
+    case 64: return tma ? launch_decode_dt<64, true, 128, KV, 32>(p, tk, tv, num_items, s)
+                        : launch_decode_dt<64, false, 128, KV, 32>(p, tk, tv, num_items, s);
+    case 128: return tma ? launch_decode_dt<128, true, 128, KV, 32>(p, tk, tv, num_items, s)
+                         : launch_decode_dt<128, false, 128, KV, 32>(p, tk, tv, num_items, s);
     case 256: return tma ? launch_decode_dt<256, true, 64, KV>(p, tk, tv, num_items, s)
                          : launch_decode_dt<256, false, 64, KV>(p, tk, tv, num_items, s);
     default: return cudaErrorInvalidValue;

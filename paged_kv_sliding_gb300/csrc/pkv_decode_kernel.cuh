@@ -41,20 +41,21 @@ namespace dec {
 // KV = element type of the caches: PKV_BF16, PKV_FP8_E4M3 or PKV_FP8_E5M2. An 8-bit
 // tile takes half the bytes, so the ring holds twice the stages (the same bytes in
 // flight per SM).
-template <int D, int TT, int KV = PKV_BF16>
+template <int D, int TT, int KV = PKV_BF16, int TPW = 16>
 struct DecTraits {
     static constexpr int kElem = KV == PKV_BF16 ? 2 : 1;  // bytes per cache element
     static constexpr int kRowBytes = D * kElem;            // one token of one head
     static constexpr int kPlaneRow = kRowBytes < 128 ? kRowBytes : 128;  // bytes per row of a plane
     static constexpr int kTile = TT;
-    static constexpr int kCompute = TT / 16;  // compute warps, 16 tokens of each tile apiece
+    static constexpr int kCompute = TT / TPW;  // compute warps, TPW tokens of each tile apiece
     static constexpr int kThreads = 32 * (kCompute + 1);  // + one producer warp
     static constexpr int kNCh = kRowBytes / kPlaneRow;    // swizzled column planes
     static constexpr int kGran = kRowBytes / 16;          // 16-byte granules per row
     static constexpr int kPlaneBytes = kTile * kPlaneRow;
     static constexpr int kTileBytes = kTile * kRowBytes;  // K or V of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = (D == 64 ? 4 : 3) * (kElem == 1 ? 2 : 1);
+    // Stages: about the same bytes in flight per SM for every variant.
+    static constexpr int kStages = TT == 128 ? 3 : (D == 64 ? 4 : 3) * (kElem == 1 ? 2 : 1);
     static constexpr int kORowFloats = D + 8;  // padded row of the combine buffer
     static constexpr int kCombineBytes = kCompute * kDecodeRows * kORowFloats * 4;
     static constexpr int kRingBytes = kStages * kStageBytes;
@@ -107,12 +108,13 @@ __device__ __forceinline__ void fp8x4_pairs_to_f16x2(uint32_t w, uint32_t &even,
     }
 }
 
-template <int D, bool TMA_KV, int TT, int KV>
-__global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, TT, KV>::kMinBlocks)
+template <int D, bool TMA_KV, int TT, int KV, int TPW>
+__global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits<D, TT, KV, TPW>::kMinBlocks)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v)
 {
-    using Tr = DecTraits<D, TT, KV>;
+    using Tr = DecTraits<D, TT, KV, TPW>;
+    constexpr int NSB = TPW / 16;  // 16-token sub-blocks per compute warp
     constexpr bool KV8 = KV != PKV_BF16;
     constexpr int PR = Tr::kPlaneRow;
     constexpr int S = Tr::kStages;
@@ -348,14 +350,14 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
                 break;
             const uint32_t kb = ring + s * Tr::kStageBytes;
             const uint32_t vb = kb + Tr::kTileBytes;
-            const int wt0 = tb + t * TT + warp * 16;  // first token of this warp's 16
-            const bool partial = wt0 < it.j0 || wt0 + 16 > it.j1;
+            const int wt0 = tb + t * TT + warp * TPW;  // first token of this warp's TPW
+            const bool partial = wt0 < it.j0 || wt0 + TPW > it.j1;
             if (TMA_KV && partial) {
                 // V rows outside [j0, j1) hold other keys, foreign slots or stale
                 // data: zero them so that P = 0 never meets a non-finite value.
                 uint8_t *vgen = ring_gen + s * Tr::kStageBytes + Tr::kTileBytes;
-                for (int e = lane; e < 16 * Tr::kGran; e += 32) {
-                    const int row = warp * 16 + e / Tr::kGran, c = e % Tr::kGran;
+                for (int e = lane; e < TPW * Tr::kGran; e += 32) {
+                    const int row = warp * TPW + e / Tr::kGran, c = e % Tr::kGran;
                     const int j = tb + t * TT + row;
                     if (j < it.j0 || j >= it.j1)
                         *reinterpret_cast<uint4 *>(vgen + plane_off<TT, PR>(row, c)) = make_uint4(0, 0, 0, 0);
@@ -363,37 +365,48 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
                 __syncwarp();
             }
 
-            // Even and odd k-steps accumulate apart (sc, sc2) and are added at the end:
-            // half the length of the dependent MMA chain.
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            if (!KV8) {
+            // S for each 16-token sub-block b of the warp: even and odd k-steps
+            // accumulate apart (sc, sc2) and are added at the end, which halves the
+            // dependent MMA chain; the sub-blocks are independent chains.
+            float sc[NSB][2][4], sc2[NSB][2][4];
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const int mi = lane >> 3;
-                    const int row = warp * 16 + ((mi >> 1) << 3) + (lane & 7);
-                    const int c16 = 2 * ks + (mi & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(kb + plane_off<TT>(row, c16), b0, b1, b2, b3);
-                    float (&acc)[2][4] = (ks & 1) ? sc2 : sc;
-                    mma_bf16_16816(acc[0], qf[ks], b0, b1);
-                    mma_bf16_16816(acc[1], qf[ks], b2, b3);
-                }
-            } else {
-                // One 16-byte granule of an 8-bit K row = the 16 columns of one k-step.
-                // Matrix m of the x4 load: tokens 8(m & 1) .. +7, granule 2kk + (m >> 1);
-                // each word holds token lane/4's columns 4c .. 4c+3.
+            for (int b = 0; b < NSB; ++b)
 #pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
-                    const int mi = lane >> 3;
-                    const int row = warp * 16 + ((mi & 1) << 3) + (lane & 7);
-                    uint32_t w[4];
-                    ldmatrix_x4(kb + plane_off<TT, PR>(row, 2 * kk + (mi >> 1)), w[0], w[1], w[2], w[3]);
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        uint32_t b0, b1;
-                        fp8x4_to_f16x2<KV>(w[m], b0, b1);
-                        mma_f16_16816((m >> 1) ? sc2[m & 1] : sc[m & 1], qf[2 * kk + (m >> 1)], b0, b1);
+                    for (int e = 0; e < 4; ++e)
+                        sc[b][nt][e] = sc2[b][nt][e] = 0.f;
+#pragma unroll
+            for (int b = 0; b < NSB; ++b) {
+                const int row0 = warp * TPW + 16 * b;
+                if (!KV8) {
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const int mi = lane >> 3;
+                        const int row = row0 + ((mi >> 1) << 3) + (lane & 7);
+                        const int c16 = 2 * ks + (mi & 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4(kb + plane_off<TT>(row, c16), b0, b1, b2, b3);
+                        float (&acc)[2][4] = (ks & 1) ? sc2[b] : sc[b];
+                        mma_bf16_16816(acc[0], qf[ks], b0, b1);
+                        mma_bf16_16816(acc[1], qf[ks], b2, b3);
+                    }
+                } else {
+                    // One 16-byte granule of an 8-bit K row = the 16 columns of one
+                    // k-step. Matrix m of the x4 load: tokens 8(m & 1) .. +7, granule
+                    // 2kk + (m >> 1); each word holds token lane/4's columns 4c .. 4c+3.
+#pragma unroll
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const int mi = lane >> 3;
+                        const int row = row0 + ((mi & 1) << 3) + (lane & 7);
+                        uint32_t w[4];
+                        ldmatrix_x4(kb + plane_off<TT, PR>(row, 2 * kk + (mi >> 1)), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            uint32_t b0, b1;
+                            fp8x4_to_f16x2<KV>(w[m], b0, b1);
+                            mma_f16_16816((m >> 1) ? sc2[b][m & 1] : sc[b][m & 1], qf[2 * kk + (m >> 1)], b0, b1);
+                        }
                     }
                 }
             }
@@ -401,30 +414,41 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
             // scaled dot (a uniform branch); then the mask, on the edge tiles only.
             if (p.cap_in > 0.f) {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int b = 0; b < NSB; ++b)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        sc[nt][e] = cap_scale * soft_cap_tanh((sc[nt][e] + sc2[nt][e]) * cap_in);
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            sc[b][nt][e] = cap_scale * soft_cap_tanh((sc[b][nt][e] + sc2[b][nt][e]) * cap_in);
             } else {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int b = 0; b < NSB; ++b)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        sc[nt][e] = (sc[nt][e] + sc2[nt][e]) * scale;
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            sc[b][nt][e] = (sc[b][nt][e] + sc2[b][nt][e]) * scale;
             }
             if (partial) {
-                const int tok_base = wt0 + 2 * (lane & 3);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int b = 0; b < NSB; ++b) {
+                    const int tok_base = wt0 + 16 * b + 2 * (lane & 3);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = tok_base + nt * 8 + (e & 1);
-                        if (j < it.j0 || j >= it.j1)
-                            sc[nt][e] = -INFINITY;
-                    }
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = tok_base + nt * 8 + (e & 1);
+                            if (j < it.j0 || j >= it.j1)
+                                sc[b][nt][e] = -INFINITY;
+                        }
+                }
             }
-            float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-            float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int b = 0; b < NSB; ++b) {
+                mx0 = fmaxf(mx0, fmaxf(fmaxf(sc[b][0][0], sc[b][0][1]), fmaxf(sc[b][1][0], sc[b][1][1])));
+                mx1 = fmaxf(mx1, fmaxf(fmaxf(sc[b][0][2], sc[b][0][3]), fmaxf(sc[b][1][2], sc[b][1][3])));
+            }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
@@ -435,16 +459,21 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
             const float a0 = fast_exp2(m[0] - ref0), a1 = fast_exp2(m[1] - ref1);
             m[0] = mn0;
             m[1] = mn1;
-            float pr[2][4];
+            // P = 2^(s - m) overwrites the scores
+            float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                pr[nt][0] = fast_exp2(sc[nt][0] - ref0);
-                pr[nt][1] = fast_exp2(sc[nt][1] - ref0);
-                pr[nt][2] = fast_exp2(sc[nt][2] - ref1);
-                pr[nt][3] = fast_exp2(sc[nt][3] - ref1);
-            }
-            l[0] = l[0] * a0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
-            l[1] = l[1] * a1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+            for (int b = 0; b < NSB; ++b)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    sc[b][nt][0] = fast_exp2(sc[b][nt][0] - ref0);
+                    sc[b][nt][1] = fast_exp2(sc[b][nt][1] - ref0);
+                    sc[b][nt][2] = fast_exp2(sc[b][nt][2] - ref1);
+                    sc[b][nt][3] = fast_exp2(sc[b][nt][3] - ref1);
+                    ls0 += sc[b][nt][0] + sc[b][nt][1];
+                    ls1 += sc[b][nt][2] + sc[b][nt][3];
+                }
+            l[0] = l[0] * a0 + ls0;
+            l[1] = l[1] * a1 + ls1;
             // O is rescaled only when a row maximum of the warp moved (a = 1 otherwise:
             // skipping the multiply changes nothing).
             if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
@@ -456,40 +485,45 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
                     o[i][3] *= a1;
                 }
             }
-            if (!KV8) {
-                const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
-                                        pack_bf16(pr[1][0], pr[1][1]), pack_bf16(pr[1][2], pr[1][3])};
 #pragma unroll
-                for (int np = 0; np < D / 16; ++np) {
-                    const int mi = lane >> 3;
-                    const int row = warp * 16 + ((mi & 1) << 3) + (lane & 7);
-                    const int c16 = 2 * np + (mi >> 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4_trans(vb + plane_off<TT>(row, c16), b0, b1, b2, b3);
-                    mma_bf16_16816(o[2 * np], pa, b0, b1);
-                    mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
-                }
-            } else {
-                // P in f16 (values in [0, 1]). A transposed x4 load of the 8-bit V tile
-                // gives, per word, tokens 2c and 2c+1 (c = lane & 3) of columns 2n, 2n+1
-                // (n = lane / 4) of one granule; a byte permute pairs the two tokens of
-                // each column. o[2g] then accumulates the even columns 16g + 2n of
-                // granule g, o[2g + 1] the odd ones.
-                const uint32_t pa[4] = {pack_f16(pr[0][0], pr[0][1]), pack_f16(pr[0][2], pr[0][3]),
-                                        pack_f16(pr[1][0], pr[1][1]), pack_f16(pr[1][2], pr[1][3])};
+            for (int b = 0; b < NSB; ++b) {
+                const int row0 = warp * TPW + 16 * b;
+                const float (&pr)[2][4] = sc[b];
+                if (!KV8) {
+                    const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
+                                            pack_bf16(pr[1][0], pr[1][1]), pack_bf16(pr[1][2], pr[1][3])};
 #pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
-                    const int mi = lane >> 3;
-                    const int row = warp * 16 + ((mi & 1) << 3) + (lane & 7);
-                    uint32_t w[4];
-                    ldmatrix_x4_trans(vb + plane_off<TT, PR>(row, 2 * kk + (mi >> 1)), w[0], w[1], w[2], w[3]);
+                    for (int np = 0; np < D / 16; ++np) {
+                        const int mi = lane >> 3;
+                        const int row = row0 + ((mi & 1) << 3) + (lane & 7);
+                        const int c16 = 2 * np + (mi >> 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4_trans(vb + plane_off<TT>(row, c16), b0, b1, b2, b3);
+                        mma_bf16_16816(o[2 * np], pa, b0, b1);
+                        mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+                    }
+                } else {
+                    // P in f16 (values in [0, 1]). A transposed x4 load of the 8-bit V
+                    // tile gives, per word, tokens 2c and 2c+1 (c = lane & 3) of columns
+                    // 2n, 2n+1 (n = lane / 4) of one granule; a byte permute pairs the two
+                    // tokens of each column. o[2g] then accumulates the even columns
+                    // 16g + 2n of granule g, o[2g + 1] the odd ones.
+                    const uint32_t pa[4] = {pack_f16(pr[0][0], pr[0][1]), pack_f16(pr[0][2], pr[0][3]),
+                                            pack_f16(pr[1][0], pr[1][1]), pack_f16(pr[1][2], pr[1][3])};
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {  // granule 2kk + h: words 2h (tokens 0-7), 2h+1 (8-15)
-                        uint32_t e0, o0, e1, o1;
-                        fp8x4_pairs_to_f16x2<KV>(w[2 * h], e0, o0);
-                        fp8x4_pairs_to_f16x2<KV>(w[2 * h + 1], e1, o1);
-                        mma_f16_16816(o[4 * kk + 2 * h], pa, e0, e1);
-                        mma_f16_16816(o[4 * kk + 2 * h + 1], pa, o0, o1);
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const int mi = lane >> 3;
+                        const int row = row0 + ((mi & 1) << 3) + (lane & 7);
+                        uint32_t w[4];
+                        ldmatrix_x4_trans(vb + plane_off<TT, PR>(row, 2 * kk + (mi >> 1)), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {  // granule 2kk + h: words 2h (tokens 0-7), 2h+1 (8-15)
+                            uint32_t e0, o0, e1, o1;
+                            fp8x4_pairs_to_f16x2<KV>(w[2 * h], e0, o0);
+                            fp8x4_pairs_to_f16x2<KV>(w[2 * h + 1], e1, o1);
+                            mma_f16_16816(o[4 * kk + 2 * h], pa, e0, e1);
+                            mma_f16_16816(o[4 * kk + 2 * h + 1], pa, o0, o1);
+                        }
                     }
                 }
             }
@@ -671,14 +705,14 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV>::kThreads, DecTraits<D, T
     }
 }
 
-template <int D, bool TMA_KV, int TT, int KV>
+template <int D, bool TMA_KV, int TT, int KV, int TPW = 16>
 cudaError_t launch_decode_dt(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int num_items,
                              cudaStream_t s)
 {
-    using Tr = DecTraits<D, TT, KV>;
+    using Tr = DecTraits<D, TT, KV, TPW>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, TMA_KV, TT, KV>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, TMA_KV, TT, KV, TPW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kDynSmem);
         if (e != cudaSuccess)
             return e;
@@ -697,7 +731,7 @@ cudaError_t launch_decode_dt(const DecodeParams &p, const CUtensorMap &tk, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<D, TMA_KV, TT, KV>, p, tk, tv);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, TMA_KV, TT, KV, TPW>, p, tk, tv);
 }
 
 }  // namespace dec

@@ -178,8 +178,15 @@ inline int decode_tile_for(int head_dim, int64_t max_keys, int64_t n_items, int 
         return 32;
     return 64;
 }
-// Page sizes whose pages the decode kernel loads with TMA boxes.
-bool decode_tma_page_size(int page_size);
+// KV tokens per stage of the decode kernel that runs a plan's tile variant (32: short
+// key ranges; 64: the rest): 8-bit caches at head_dim <= 128 run the long variant with
+// 128-token stages, two 16-token sub-blocks per compute warp.
+inline int decode_kernel_tile(int tile, int head_dim, int kv_dtype)
+{
+    return (tile == 64 && kv_dtype != PKV_BF16 && head_dim <= 128) ? 128 : tile;
+}
+// Page sizes whose pages the decode kernel loads with TMA boxes of a `tile`-token stage.
+bool decode_tma_page_size(int page_size, int tile);
 // 4-D tensor map [page, slot, KV head, d] over a cache of kv_dtype elements, boxes of
 // one 128-byte plane (64 bytes for 8-bit d 64) x box_rows slots.
 bool encode_kv_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_heads, int page_size,
