@@ -385,7 +385,7 @@ def run_ours(args, rank, world):
 
 
 EXTRA = ("swa_prefill_p1", "swa_prefill_p16", "extend_prefix", "extend_ragged", "long_decode",
-         "batch_decode_fp8", "long_decode_fp8")
+         "batch_decode_fp8", "long_decode_fp8", "extend_prefix_fp8")
 
 
 def bench_prefill_ragged(pkv, w, steps, warmup, flush):
@@ -430,6 +430,13 @@ def extra_workloads(pkv, args, peaks, flush, only=None):
         r = bench_prefill(pkv, w, steps, 3, flush)
         r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
         res["extend_prefix_16req_W4095"] = r
+        del w
+        torch.cuda.empty_cache()
+    if want("extend_prefix_fp8"):
+        w = wl.to_kv8(wl.extend_with_prefix(device="cuda"), "e4m3")
+        r = bench_prefill(pkv, w, steps, 3, flush)
+        r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]  # f16 MMAs run at the bf16 rate
+        res["extend_prefix_16req_W4095_e4m3"] = r
         del w
         torch.cuda.empty_cache()
     if want("extend_ragged"):

@@ -88,7 +88,7 @@ typedef enum pkv_kind {
 typedef enum pkv_dtype {
     PKV_BF16 = 0,
     PKV_F32 = 1,     /* merge_state values only */
-    PKV_FP8_E4M3 = 2, /* 8-bit K/V caches (pkv_plan_desc.kv_dtype, DECODE plans): OCP E4M3,
+    PKV_FP8_E4M3 = 2, /* 8-bit K/V caches (pkv_plan_desc.kv_dtype, paged plans): OCP E4M3,
                          torch.float8_e4m3fn */
     PKV_FP8_E5M2 = 3  /* OCP E5M2, torch.float8_e5m2 */
 } pkv_dtype;
@@ -133,12 +133,12 @@ typedef struct pkv_plan_desc {
     float logits_soft_cap;
     float k_scale;
     float v_scale;
-    /* Element type of k_cache and v_cache: PKV_BF16 (0), or for DECODE plans an 8-bit
-     * float, PKV_FP8_E4M3 or PKV_FP8_E5M2 (flashinfer_backend.py, should_use_tensor_core,
-     * names torch.float8_e4m3fn and torch.float8_e5m2 as KV cache dtypes). The caches
-     * then hold one byte per element in the same [num_pages, page_size, H_kv, d]
-     * layout, K = k_scale * (stored value) and V = v_scale * (stored value); q and out
-     * stay bf16. PREFILL plans with an 8-bit cache return PKV_ERR_UNSUPPORTED. */
+    /* Element type of k_cache and v_cache: PKV_BF16 (0), or an 8-bit float,
+     * PKV_FP8_E4M3 or PKV_FP8_E5M2 (flashinfer_backend.py, should_use_tensor_core, names
+     * torch.float8_e4m3fn and torch.float8_e5m2 as KV cache dtypes). The caches then
+     * hold one byte per element in the same [num_pages, page_size, H_kv, d] layout,
+     * K = k_scale * (stored value) and V = v_scale * (stored value); q and out stay
+     * bf16. PREFILL_RAGGED plans take bf16 K/V only (PKV_ERR_UNSUPPORTED otherwise). */
     int32_t kv_dtype;
 } pkv_plan_desc;
 

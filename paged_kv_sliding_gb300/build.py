@@ -22,6 +22,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
 
 SOURCES = ["pkv_api.cpp", "pkv_decode.cu", "pkv_decode_fp8.cu", "pkv_merge.cu", "pkv_prefill.cu",
+           "pkv_prefill_fp8.cu",
            "pkv_noalloc.cu", "pkv_indices.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -41,7 +42,7 @@ def _flags(extra_verbose=False):
 # Kernels that redistribute registers between warpgroups with setmaxnreg: the
 # launch allocation (threads x registers per thread) must be exactly what the
 # split assumes, or setmaxnreg.inc would wait for registers that never come.
-REGISTER_SPLIT = {"pkv_prefill.cu": ("prefill_pp_kernel", 168)}
+REGISTER_SPLIT = {"pkv_prefill.cu": ("prefill_pp_kernel", 168), "pkv_prefill_fp8.cu": ("prefill_pp_kernel", 168)}
 
 
 def _check_register_split(logs):

@@ -120,8 +120,8 @@ int validate(const pkv_plan_desc *d, std::vector<HostRequest> &reqs)
     if (d->kv_dtype != PKV_BF16 && d->kv_dtype != PKV_FP8_E4M3 && d->kv_dtype != PKV_FP8_E5M2)
         return fail(PKV_ERR_INVALID_ARG, "kv_dtype %d is not PKV_BF16, PKV_FP8_E4M3 or PKV_FP8_E5M2",
                     d->kv_dtype);
-    if (d->kv_dtype != PKV_BF16 && d->kind != PKV_DECODE)
-        return fail(PKV_ERR_UNSUPPORTED, "8-bit K/V caches are supported by DECODE plans only");
+    if (d->kv_dtype != PKV_BF16 && d->kind == PKV_PREFILL_RAGGED)
+        return fail(PKV_ERR_UNSUPPORTED, "8-bit K/V are supported in paged caches only");
     if (!(d->sm_scale == d->sm_scale) || std::isinf(d->sm_scale))
         return fail(PKV_ERR_INVALID_ARG, "sm_scale is not finite");
     if (!(d->sm_scale > 0.f))
@@ -324,9 +324,10 @@ void build_schedule(const pkv_plan_desc &d, const std::vector<HostRequest> &reqs
         const int tq = prefill_tokens_per_cta(d.head_dim, group);
         // Ragged K/V: a TMA box may start at any row. Pages: at a page (TMA page
         // boxes) or anywhere (cp.async gathers).
-        const int64_t kv_align = d.kind == PKV_PREFILL_RAGGED                        ? 1
-                                 : prefill_pp_tma_page_size(d.page_size, d.head_dim) ? std::min(d.page_size, T)
-                                                                                     : 1;
+        // 8-bit caches are gathered row by row.
+        const int64_t kv_align = d.kind == PKV_PREFILL_RAGGED || d.kv_dtype != PKV_BF16 ? 1
+                                 : prefill_pp_tma_page_size(d.page_size, d.head_dim)    ? std::min(d.page_size, T)
+                                                                                        : 1;
         for (int b = 0; b < B; ++b) {
             const HostRequest &r = reqs[b];
             for (int64_t t0 = 0; t0 < r.qo_len; t0 += tq) {
@@ -904,6 +905,7 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.cap_out = lf.cap_out;
     p.v_scale = lf.v_scale;
     p.ragged = d.kind == PKV_PREFILL_RAGGED ? 1 : 0;
+    p.kv_dtype = d.kv_dtype;
     p.total_kv = (int32_t)plan->total_kv;
     if (p.ragged) {
         p.page_size = 1;

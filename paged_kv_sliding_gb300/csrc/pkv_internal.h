@@ -141,6 +141,7 @@ struct PrefillParams {
     float v_scale;
     int32_t ragged;          // 1: K/V are contiguous [total_kv, H_kv, d], kv_page_begin = token offset
     int32_t total_kv;        // ragged: rows of K/V (bound of their tensor maps)
+    int32_t kv_dtype;        // element type of the caches (pkv_dtype: bf16 or an 8-bit float)
 };
 
 // The logit and output factors of a plan descriptor (k_scale folded into the logit
@@ -203,6 +204,9 @@ cudaError_t launch_prefill_pp(const PrefillParams &p, int head_dim, int mask_mod
                               cudaStream_t s);
 // Page sizes whose pages the prefill kernel loads with TMA boxes.
 bool prefill_pp_tma_page_size(int page_size, int head_dim);
+// The prefill kernels over 8-bit caches (p.kv_dtype = PKV_FP8_E4M3 or PKV_FP8_E5M2).
+cudaError_t launch_prefill_pp_kv8(const PrefillParams &p, int head_dim, int mask_mode, int num_ctas,
+                                  cudaStream_t s);
 
 // Set the calling thread's pkv_last_error() text.
 void set_last_error(const char *msg);

@@ -1,0 +1,983 @@
+// Paged prefill / extend kernel on the 5th-generation tensor cores: for head_dim
+// 64 and 128 two 128-row query tiles per work item ping-pong over 128-key tiles;
+// for head_dim 256 (whose O accumulator takes half of TMEM) one query tile per
+// work item runs over 64-key tiles.
+//
+// Method: plan-clipped KV tiles (the tile-granular KV-start skip of sglang PR
+// #31501), the exact per-element mask on boundary tiles, fp32 online softmax with
+// lazily rescaled O. Laid out for throughput:
+//   * persistent: one CTA per SM walks its own list of work items (balanced by the
+//     plan), so TMEM allocation, barrier set-up and the K/V ring are paid once per
+//     CTA, the next item's Q and first K/V tiles land while the current item
+//     finishes, and an item's epilogue overlaps the next item's first S = Q K^T;
+//   * two query tiles Q0, Q1 (256 packed rows) share every K/V tile, halving K/V
+//     traffic per flop (head_dim 64 and 128);
+//   * P is written back into TMEM over the first half of its own S columns (bf16,
+//     two per column) and consumed by tcgen05.mma with the A operand in TMEM, so no
+//     shared memory is spent on P;
+//   * K and V tiles stream through a ring of 5 (head_dim 128, 256) or 8 (head_dim
+//     64) shared-memory slots, filled by TMA (a 4-D tensor map over the page pool,
+//     one box per page and 64-column chunk) when the page size is a multiple of 8
+//     that divides the KV tile (or is a multiple of it), else by cp.async
+//     gathers; Q always arrives by TMA (4-D map over [token, KV head, group, d]);
+//   * one thread issues, per KV tile j: S0(j) = Q0 K_j^T, O1 += P1(j-1) V_{j-1},
+//     S1(j) = Q1 K_j^T, O0 += P0(j) V_j, so the tensor core works on one query
+//     tile while the softmax warpgroup of the other runs. Tensor-core operations of
+//     one thread execute in issue order, which makes S_i(j) complete only after
+//     O_i += P_i(j-1) V, the ordering every TMEM reuse below relies on.
+// Warps (384 threads): 0-3 softmax + epilogue of Q0, 4-7 of Q1 (thread = TMEM
+// lane = packed row), 8 TMEM allocation, Q loads and MMA issue (one lane), 9 TMA
+// producer of K/V (9-11 gather with cp.async in the other mode).
+// Every wait is bounded (PKV_ERR_TIMEOUT, abort flag, MMA drain, TMEM freed).
+//
+// 8-bit K/V caches (E4M3 / E5M2): warps 9-11 copy the 8-bit rows with cp.async into a
+// two-tile staging area and widen them to f16 into the ring; both MMAs run on f16
+// operands (every E4M3 / E5M2 value is exact in f16). Each softmax warpgroup writes
+// its own Q tile for the next item as f16 with every row scaled by a power of two
+// (max |q| * 2^e in [2^13, 2^14)) and scales that row's logits back by 2^-e; P goes to
+// the PV MMA as f16.
+#pragma once
+
+#include <cfloat>
+#include <climits>
+
+#include "pkv_internal.h"
+#include "pkv_sm100.cuh"
+
+namespace pkv {
+namespace pp {
+
+template <int D, bool KV8 = false>
+struct PPTraits {
+    static constexpr int kM = 128;            // packed rows per query tile
+    static constexpr int kT = D >= 256 ? 64 : 128;  // KV tokens per tile
+    static constexpr int kNQ = D >= 256 ? 1 : 2;    // query tiles per CTA (TMEM: S_i, O_i)
+    static constexpr int kChunk = 128;        // bytes per swizzled row
+    static constexpr int kNCh = D / 64;       // 64-column chunks
+    static constexpr int kQTileBytes = kM * D * 2;
+    static constexpr int kSlotBytes = kT * D * 2;
+    // 8-bit caches: fewer f16 slots, and two staging tiles of 8-bit K and V rows.
+    static constexpr int kSlots = KV8 ? (D == 64 ? 6 : 3) : (D == 64 ? 8 : 5);
+    static constexpr int kStgTileBytes = KV8 ? 2 * kT * D : 0;  // K rows, then V rows
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffSlots = kNQ * kQTileBytes;
+    static constexpr int kOffStg = kOffSlots + kSlots * kSlotBytes;
+    static constexpr int kDynSmem = kOffStg + 2 * kStgTileBytes + 1024;
+    static constexpr int kThreads = 384;
+    static constexpr int kProducers = 96;     // cp.async mode: warps 9-11
+    static constexpr int kIdsPerTile = kT;    // page-id ring entries per tile (one per row)
+    static constexpr int kTmemCols = 512;
+    static constexpr int kTmemO = 256;        // O_i at kTmemO + i * D; S_i at i * kT
+    static_assert(kTmemO + kNQ * D <= kTmemCols && kNQ * kT <= kTmemO, "TMEM budget");
+};
+
+constexpr long long kWaitLimitPP = 4000000000LL;
+// Page-id ring of the cp.async producers, in tiles (ids of kIdRing - 1 tiles in flight).
+constexpr int kIdRing = 3;
+
+// K and V of a KV tile complete one barrier, the K slot's: a slot's barrier then
+// completes one phase per use of the slot as a K slot. K tiles sit at the even
+// ring positions, so with an even slot count every use of an even slot is a K use
+// (a phase every NS positions) and with an odd count every other use is (a phase
+// every 2 NS positions).
+template <int NS>
+__host__ __device__ constexpr int full_period() { return NS % 2 == 0 ? NS : 2 * NS; }
+constexpr int kRegsLaunch = 168;   // 65536 / 384 rounded down to a multiple of 8
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsOther = 96;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * kRegsLaunch, "register split");
+
+template <int NS>
+struct PPBars {
+    static constexpr int kQ = 0;
+    static constexpr int kFull = 1;              // NS: K and V of a tile landed (on the K slot's barrier)
+    static constexpr int kEmpty = kFull + NS;
+    static constexpr int kSFull = kEmpty + NS;   // 2: S_i(j) complete in TMEM
+    static constexpr int kPFull = kSFull + 2;    // 2: P_i(j) written to TMEM (128 arrivals)
+    static constexpr int kOFinal = kPFull + 2;   // 2: O_i of the item complete
+    static constexpr int kOEmpty = kOFinal + 2;  // 2: O_i read out by the epilogue (128 arrivals)
+    static constexpr int kVLand = kOEmpty + 2;   // producer only: a tail V tile has landed
+    static constexpr int kDrain = kVLand + 1;
+    static constexpr int kQ1 = kDrain + 1;       // 8-bit caches: Q_1 written (128 arrivals; kQ: Q_0)
+    static constexpr int kCount = kQ1 + 1;
+};
+
+template <int D, int MASK, bool TMA_KV, bool RAGGED, int KV = PKV_BF16>
+__global__ void __launch_bounds__(384, 1)
+    prefill_pp_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
+{
+    constexpr bool KV8 = KV != PKV_BF16;
+    static_assert(!KV8 || (!TMA_KV && !RAGGED), "8-bit caches are gathered by the cp.async producers");
+    using Tr = PPTraits<D, KV8>;
+    constexpr int NS = Tr::kSlots;
+    using B = PPBars<NS>;
+    constexpr int kFullPeriod = full_period<NS>();
+    constexpr int T = Tr::kT;
+    constexpr int NCH = Tr::kNCh;
+    constexpr int CH = D / 8;
+    constexpr bool kCausal = MASK == kMaskCausal || MASK == kMaskCausalWindow;
+    constexpr bool kWindow = MASK == kMaskCausalWindow || MASK == kMaskWindow;
+
+    extern __shared__ uint8_t dsmem_raw[];
+    __shared__ __align__(8) uint64_t bars[B::kCount];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_flag;
+    __shared__ int no_abort;
+    __shared__ int id_ring[(TMA_KV || KV8) ? 1 : kIdRing * Tr::kIdsPerTile];
+
+    const uint32_t base = (smem_u32(dsmem_raw) + 1023u) & ~1023u;
+    const uint32_t sQ = base + Tr::kOffQ;
+    const uint32_t sSlots = base + Tr::kOffSlots;
+    const uint32_t sStg = base + Tr::kOffStg;  // 8-bit caches only
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    auto slot = [&](int s) { return sSlots + (uint32_t)s * Tr::kSlotBytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // This CTA's work items, in order (the plan balances the lists over the CTAs).
+    const int item_lo = p.cta_items[blockIdx.x];
+    const int item_hi = p.cta_items[blockIdx.x + 1];
+    const int g = p.group;
+    const int tq = p.tokens_per_tile;  // query tokens per 128-row tile
+    auto q_tiles = [&](const PrefillItem &it) { return (Tr::kNQ > 1 && it.ntok > tq) ? 2 : 1; };
+    const volatile int *abort_v = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B::kQ), KV8 ? 128 : 1);
+        mbar_init(bar(B::kQ1), 128);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(B::kFull + s), TMA_KV ? 1 : Tr::kProducers);
+            mbar_init(bar(B::kEmpty + s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B::kSFull + i), 1);
+            mbar_init(bar(B::kPFull + i), 128);
+            mbar_init(bar(B::kOFinal + i), 1);
+            mbar_init(bar(B::kOEmpty + i), 128);
+        }
+        mbar_init(bar(B::kVLand), 1);
+        mbar_init(bar(B::kDrain), 1);
+        abort_flag = 0;
+        no_abort = 0;
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 8) {
+        tmem_alloc(smem_u32(&tmem_base_s), Tr::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    // Register split: the block is launched with 384 x 168 registers (the build
+    // checks that ptxas allocated exactly 168); the softmax warpgroups take 200 and
+    // the MMA / producer warpgroup gives back down to 96: 256 x 200 + 128 x 96 =
+    // 63488 <= 64512.
+    if (warp >= 8)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsOther));
+    else
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsSoftmax));
+
+    if (warp < 8) {
+        // ------------------------------------------------------------ softmax
+        const int wg = warp >> 2;
+        const int r = threadIdx.x & 127;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + wg * T;
+        const uint32_t tO = tmem + lane_off + Tr::kTmemO + wg * D;
+        float scale = p.sm_scale_log2;  // raw dot (or capped logit) -> log2-domain logit
+        float cap_in = p.cap_in;         // raw dot -> tanh argument
+        uint32_t n_s = 0;  // S_wg tiles consumed so far: the phase of SFull / PFull
+        uint32_t n_o = 0;  // items accumulated into O_wg so far: the phase of OFinal / OEmpty
+        bool ok = true;
+        // 8-bit caches: the next item whose Q_wg this warpgroup writes (an item with
+        // KV tiles that uses query tile wg), and the scale-back of this thread's row.
+        auto next_q_item = [&](int ii) {
+            while (ii < item_hi && (p.items[ii].kv_tiles <= 0 || wg >= q_tiles(p.items[ii])))
+                ++ii;
+            return ii;
+        };
+        // Row r of Q_wg for item qi: q scaled by 2^e (e from the row's max |q|), as f16,
+        // in the 128-byte-swizzled K-major layout of the S MMA's A operand; rows past
+        // the item's tokens are zero. Q_wg is free: the S_wg MMAs of the previous item,
+        // its only readers, completed before their last S was consumed.
+        auto write_q = [&](int qi) -> float {
+            const PrefillItem qit = p.items[qi];
+            const int nt = min(tq, qit.ntok - wg * tq);
+            const bool valid = r < nt * g;
+            const int tok = qit.tok0 + wg * tq + r / g;
+            const int h = qit.kv_head * g + r % g;
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                p.q + ((size_t)(p.reqs[qit.req].qo_begin + (valid ? tok : 0)) * p.num_qo_heads + h) * D);
+            float amax = 0.f;
+            if (valid) {
+#pragma unroll 4
+                for (int k = 0; k < D / 8; ++k) {
+                    const uint4 v = __ldg(src + k);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        amax = max3f(amax, fabsf(__uint_as_float(w4[e] << 16)),
+                                     fabsf(__uint_as_float(w4[e] & 0xffff0000u)));
+                }
+            }
+            int qe = 13 - ((int)((__float_as_uint(amax) >> 23) & 0xff) - 127);
+            qe = qe < -100 ? -100 : (qe > 100 ? 100 : qe);
+            const float up = __uint_as_float((uint32_t)(127 + qe) << 23);
+            const uint32_t qtile = sQ + wg * Tr::kQTileBytes;
+#pragma unroll 4
+            for (int k = 0; k < D / 8; ++k) {
+                const uint4 v = valid ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                uint32_t f[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    f[e] = pack_f16(__uint_as_float(w4[e] << 16) * up, __uint_as_float(w4[e] & 0xffff0000u) * up);
+                const uint32_t a = qtile + (k >> 3) * (128 * Tr::kChunk) + r * Tr::kChunk + (((k & 7) ^ (r & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(f[0]), "r"(f[1]), "r"(f[2]),
+                             "r"(f[3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(wg == 0 ? B::kQ : B::kQ1));
+            return __uint_as_float((uint32_t)(127 - qe) << 23);
+        };
+        int q_item = item_hi;
+        float q_unscale = 1.f;
+        if (KV8) {
+            q_item = next_q_item(item_lo);
+            if (q_item < item_hi)
+                q_unscale = write_q(q_item);
+        }
+        for (int ii = item_lo; ok && ii < item_hi; ++ii) {
+            const PrefillItem it = p.items[ii];
+            if (wg >= q_tiles(it))
+                continue;
+            if (KV8 && it.kv_tiles > 0) {
+                // this item is q_item: its logits carry the row's 2^e
+                scale = p.cap_in > 0.f ? p.sm_scale_log2 : p.sm_scale_log2 * q_unscale;
+                cap_in = p.cap_in * q_unscale;
+            }
+            const RequestInfo rq = p.reqs[it.req];
+            const int n_tiles = it.kv_tiles;
+            const int ntok_wg = min(tq, it.ntok - wg * tq);
+            const int tok = it.tok0 + wg * tq + r / g;
+            const int pos = rq.q_start + tok;
+            const int p_min = rq.q_start + it.tok0 + wg * tq;
+            const int p_max = p_min + ntok_wg - 1;
+            float m_used = -INFINITY;
+            float l = 0.f;
+            for (int j = 0; j < n_tiles; ++j, ++n_s) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull + wg), n_s & 1, abort_v, kWaitLimitPP));
+                if (!ok)
+                    break;
+                tc_fence_after();
+                float s[T];
+#pragma unroll
+                for (int c = 0; c < T / 32; ++c)
+                    tmem_ld32(tS + 32 * c, *reinterpret_cast<float(*)[32]>(&s[32 * c]));
+                tmem_wait_ld();
+                if (p.cap_in > 0.f) {
+                    // soft cap on the raw dot products, before the mask
+#pragma unroll
+                    for (int c = 0; c < T; ++c)
+                        s[c] = p.cap_out * soft_cap_tanh(s[c] * cap_in);
+                }
+
+                const int j0 = prefill_kv_key_at(it, j, T);
+                bool need_mask = j0 + T > rq.kv_len;
+                if (kCausal)
+                    need_mask |= j0 + T - 1 > p_min;
+                if (kWindow)
+                    need_mask |= j0 < p_max - p.window_left;
+                if (need_mask) {
+                    const int lo_c = kWindow ? pos - p.window_left - j0 : INT_MIN;
+                    int hi_c = rq.kv_len - 1 - j0;
+                    if (kCausal)
+                        hi_c = min(hi_c, pos - j0);
+#pragma unroll
+                    for (int c = 0; c < T; ++c)
+                        s[c] = (c >= lo_c && c <= hi_c) ? s[c] : -INFINITY;
+                }
+                // 8 independent chains of three-input maxima, then a tree: the row
+                // max costs T/2 instructions and stays off a long dependency chain.
+                float mx8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mx8[k] = max3f(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+                for (int c = 24; c + 16 <= T; c += 16)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mx8[k] = max3f(mx8[k], s[c + k], s[c + 8 + k]);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mx8[k] = fmaxf(mx8[k], s[T - 8 + k]);
+                const float m_raw = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                                          fmaxf(mx8[6], mx8[7]));
+                const float m_tile = m_raw == -INFINITY ? -INFINITY : m_raw * scale;
+                const float m_cand = fmaxf(m_used, m_tile);
+                const bool need = m_cand != -INFINITY && (m_used == -INFINITY || m_cand > m_used + 8.f);
+                const float alpha = need ? fast_exp2(m_used - m_cand) : 1.f;
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    // O_i is stable: S_i(j) completed after O_i += P_i(j-1) V.
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(tO + 32 * c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] *= alpha;
+                        tmem_st32(tO + 32 * c, o);
+                    }
+                }
+                if (need) {
+                    l *= alpha;
+                    m_used = m_cand;
+                }
+                const float nref = -(m_used == -INFINITY ? 0.f : m_used);
+                // Packed f32x2 arithmetic: one FMA and one add per two scores.
+                float rs[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+                for (int h = 0; h < T / 64; ++h) {
+                    uint32_t pw[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        float x0, x1;
+                        fma2(x0, x1, s[64 * h + 2 * k], s[64 * h + 2 * k + 1], scale, scale, nref, nref);
+                        const float e0 = fast_exp2(x0);
+                        const float e1 = fast_exp2(x1);
+                        add2(rs[k & 3][0], rs[k & 3][1], e0, e1);
+                        pw[k] = KV8 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+                    }
+                    tmem_st32u(tS + 32 * h, pw);
+                }
+                tmem_wait_st();
+                l += ((rs[0][0] + rs[0][1]) + (rs[1][0] + rs[1][1])) + ((rs[2][0] + rs[2][1]) + (rs[3][0] + rs[3][1]));
+                tc_fence_before();
+                mbar_arrive(bar(B::kPFull + wg));
+            }
+            if (KV8 && ok && n_tiles > 0) {
+                // Every S_wg of this item has been consumed: Q_wg of the next item may be
+                // written now, so that its first S MMA overlaps this item's epilogue.
+                q_item = next_q_item(ii + 1);
+                if (q_item < item_hi)
+                    q_unscale = write_q(q_item);
+            }
+            if (ok && n_tiles > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kOFinal + wg), n_o & 1, abort_v, kWaitLimitPP));
+                tc_fence_after();
+            }
+            if (!ok)
+                break;
+            const bool row_ok = r < ntok_wg * g;
+            const int h = it.kv_head * g + r % g;
+            const size_t orow = (size_t)(rq.qo_begin + tok) * p.num_qo_heads + h;
+            uint16_t *dst = p.out + orow * D;
+            const float inv = l > 0.f ? p.v_scale / l : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                if (n_tiles > 0) {
+                    tmem_ld32(tO + 32 * c, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = 0.f;
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 v;
+                        v.x = pack_bf16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
+                        v.y = pack_bf16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+                        v.z = pack_bf16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+                        v.w = pack_bf16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
+                        *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * q4) = v;
+                    }
+                }
+            }
+            if (n_tiles > 0) {
+                // O_wg has been read: the next item's first P V may overwrite it.
+                tc_fence_before();
+                mbar_arrive(bar(B::kOEmpty + wg));
+                ++n_o;
+            }
+            if (row_ok && p.lse)
+                p.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        }
+        if (!ok) {
+            record_status(p.status, PKV_ERR_TIMEOUT);
+            abort_flag = 1;
+        }
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ MMA issue
+        // One lane drives everything: Q loads, waits, MMA issue and commits.
+        if (lane == 0) {
+            const uint32_t idesc_s = KV8 ? idesc_f16_f32(128, T, false) : idesc_bf16_f32(128, T, false);
+            const uint32_t idesc_o = KV8 ? idesc_f16_f32(128, D, true) : idesc_bf16_f32(128, D, true);
+            auto issue_s = [&](int i, uint32_t kslot) {
+                const uint32_t qb = sQ + i * Tr::kQTileBytes;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t a = sdesc_sw128(qb + (k >> 2) * (128 * Tr::kChunk) + (k & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(kslot + (k >> 2) * (T * Tr::kChunk) + (k & 3) * 32, 16, 1024);
+                    umma_f16(tmem + i * T, a, b, idesc_s, k > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(B::kSFull + i));
+            };
+            auto issue_pv = [&](int i, uint32_t vslot, bool first) {
+#pragma unroll
+                for (int k = 0; k < T / 16; ++k) {
+                    const uint64_t b = sdesc_sw128(vslot + k * (16 * Tr::kChunk), T * Tr::kChunk, 1024);
+                    umma_f16_ts(tmem + Tr::kTmemO + i * D, tmem + i * T + k * 8, b, idesc_o,
+                                (!first || k > 0) ? 1u : 0u);
+                }
+            };
+            auto wait = [&](int b_idx, uint32_t parity) {
+                return mbar_wait(bar(b_idx), parity, abort_v, kWaitLimitPP);
+            };
+            // Q of an item: its tiles by TMA (4-D map over [token, KV head, group, d]).
+            auto load_q = [&](int ii) {
+                const PrefillItem it = p.items[ii];
+                const int nq = q_tiles(it);
+                const int qo_begin = p.reqs[it.req].qo_begin;
+                const uint32_t rows = (uint32_t)(g * tq);
+                mbar_arrive_expect_tx(bar(B::kQ), (uint32_t)nq * NCH * rows * Tr::kChunk);
+                for (int i = 0; i < nq; ++i)
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_4d(sQ + i * Tr::kQTileBytes + c * (128 * Tr::kChunk), &tm_q, c * 64, 0, it.kv_head,
+                                    qo_begin + it.tok0 + i * tq, bar(B::kQ));
+            };
+            // The next item at or after ii that has KV tiles (items without any
+            // only write zeros and take no part in the pipeline).
+            auto next_busy = [&](int ii) {
+                while (ii < item_hi && p.items[ii].kv_tiles <= 0)
+                    ++ii;
+                return ii;
+            };
+            if (!KV8)
+                tma_prefetch_desc(&tm_q);
+            uint32_t n_kv = 0;         // K/V ring position
+            uint32_t n_p[2] = {0, 0};  // P_i tiles consumed: the phase of PFull_i
+            uint32_t n_o[2] = {0, 0};  // items accumulated into O_i: the phase of OEmpty_i
+            uint32_t n_q = 0;          // Q loads: the phase of kQ
+            uint32_t n_q1 = 0;         // 8-bit caches: Q_1 writes, the phase of kQ1
+            bool ok = true;
+            int ii = next_busy(item_lo);
+            if (!KV8 && ii < item_hi)
+                load_q(ii);
+            while (ok && ii < item_hi) {
+                const PrefillItem it = p.items[ii];
+                const int nq = q_tiles(it);
+                const int n_tiles = it.kv_tiles;
+                const int ii_next = next_busy(ii + 1);
+                if (!(ok = wait(B::kQ, n_q & 1)))
+                    break;
+                ++n_q;
+                if (KV8 && nq == 2) {  // Q_1 is written by its own warpgroup
+                    if (!(ok = wait(B::kQ1, n_q1 & 1)))
+                        break;
+                    ++n_q1;
+                }
+                uint32_t sv_prev = 0;
+                for (int j = 0; j < n_tiles; ++j) {
+                    const uint32_t nK = n_kv, nV = n_kv + 1;
+                    n_kv += 2;
+                    const int sK = nK % NS, sV = nV % NS;
+                    if (!(ok = wait(B::kFull + sK, (nK / kFullPeriod) & 1)))
+                        break;
+                    if (!TMA_KV)
+                        fence_proxy_async_smem();
+                    tc_fence_after();
+                    issue_s(0, slot(sK));
+                    if (j > 0 && nq == 2) {
+                        if (!(ok = wait(B::kPFull + 1, n_p[1]++ & 1)))
+                            break;
+                        if (j == 1 && n_o[1] > 0 && !(ok = wait(B::kOEmpty + 1, (n_o[1] - 1) & 1)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(1, slot(sv_prev), j == 1);
+                        umma_commit(bar(B::kEmpty + sv_prev));
+                    }
+                    if (nq == 2)
+                        issue_s(1, slot(sK));
+                    umma_commit(bar(B::kEmpty + sK));
+                    if (!(ok = wait(B::kPFull + 0, n_p[0]++ & 1)))
+                        break;
+                    if (j == 0 && n_o[0] > 0 && !(ok = wait(B::kOEmpty + 0, (n_o[0] - 1) & 1)))
+                        break;
+                    tc_fence_after();
+                    // Single query tile: S_0 of the last KV tile has been consumed, so
+                    // every read of Q is done and the next item's Q may land.
+                    if (!KV8 && nq == 1 && j == n_tiles - 1 && ii_next < item_hi)
+                        load_q(ii_next);
+                    issue_pv(0, slot(sV), j == 0);
+                    if (nq == 1)
+                        umma_commit(bar(B::kEmpty + sV));
+                    if (j == n_tiles - 1)
+                        umma_commit(bar(B::kOFinal + 0));
+                    sv_prev = sV;
+                }
+                if (ok && nq == 2) {
+                    ok = wait(B::kPFull + 1, n_p[1]++ & 1);
+                    if (ok && n_tiles == 1 && n_o[1] > 0)
+                        ok = wait(B::kOEmpty + 1, (n_o[1] - 1) & 1);
+                    if (ok) {
+                        tc_fence_after();
+                        // S_1 of the last KV tile (issued after S_0) has been consumed.
+                        if (!KV8 && ii_next < item_hi)
+                            load_q(ii_next);
+                        issue_pv(1, slot(sv_prev), n_tiles == 1);
+                        umma_commit(bar(B::kEmpty + sv_prev));
+                        umma_commit(bar(B::kOFinal + 1));
+                    }
+                }
+                ++n_o[0];
+                if (nq == 2)
+                    ++n_o[1];
+                ii = ii_next;
+            }
+            if (!ok) {
+                record_status(p.status, PKV_ERR_TIMEOUT);
+                abort_flag = 1;
+            }
+            umma_commit(bar(B::kDrain));
+            mbar_wait(bar(B::kDrain), 0, &no_abort, kWaitLimitPP);
+        }
+        __syncwarp();
+    } else if (RAGGED) {
+        // ------------------------------------------------------------ TMA producer, ragged K/V
+        // K/V rows of request b are rows kv_page_begin + j of a [total_kv, H_kv, d]
+        // tensor: one box per 64-column chunk of a tile, at any row. Rows past the
+        // request's keys are the next request's (finite, masked in S, so P = 0) or
+        // past the tensor's end (filled with zeros by the copy).
+        static_assert(!RAGGED || TMA_KV, "ragged K/V are loaded by TMA");
+        if (warp == 9 && lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            uint32_t n = 0;  // K/V ring position
+            bool okp = true;
+            for (int ii = item_lo; okp && ii < item_hi; ++ii) {
+                const PrefillItem it = p.items[ii];
+                const int n_tiles = it.kv_tiles;
+                if (n_tiles <= 0)
+                    continue;
+                const int row_base = p.reqs[it.req].kv_page_begin;
+                for (int j = 0; okp && j < n_tiles; ++j) {
+                    const int row0 = row_base + prefill_kv_key_at(it, j, T);
+                    const uint32_t full = bar(B::kFull + n % NS);  // K and V of the tile complete it
+                    for (int isv = 0; isv < 2; ++isv, ++n) {
+                        const int s = n % NS;
+                        if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP)) {
+                            okp = false;
+                            break;
+                        }
+                        if (isv == 0)
+                            mbar_arrive_expect_tx(full, 2u * T * Tr::kChunk * NCH);
+                        const void *tm = isv ? (const void *)&tm_v : (const void *)&tm_k;
+                        for (int c = 0; c < NCH; ++c)
+                            tma_load_4d(slot(s) + c * (T * Tr::kChunk), tm, c * 64, it.kv_head, row0, 0, full);
+                    }
+                }
+            }
+            if (!okp) {
+                record_status(p.status, PKV_ERR_TIMEOUT);
+                abort_flag = 1;
+            }
+        }
+    } else if (TMA_KV) {
+        // ------------------------------------------------------------ TMA producer
+        if (warp == 9) {
+            const int P = p.page_size;
+            const int rows_box = P < T ? P : T;
+            const int npg = T / rows_box;
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+            }
+            uint32_t n = 0;       // K/V ring position
+            uint32_t n_land = 0;  // tail V tiles so far: the phase of kVLand
+            bool okp = true;
+            for (int ii = item_lo; okp && ii < item_hi; ++ii) {
+                const PrefillItem it = p.items[ii];
+                const int n_tiles = it.kv_tiles;
+                if (n_tiles <= 0)
+                    continue;
+                const RequestInfo rq = p.reqs[it.req];
+                const int n_pages_req = (rq.kv_len + P - 1) / P;
+                // Lane i: the physical page of the tile's i-th box, or -1.
+                auto load_id = [&](int j) -> int {
+                    if (lane >= npg)
+                        return -1;
+                    const int j0 = prefill_kv_key_at(it, j, T);
+                    const int lp = P <= T ? j0 / P + lane : j0 / P;
+                    if (lp >= n_pages_req)
+                        return -1;
+                    const int pg = __ldg(p.kv_indices + rq.kv_page_begin + lp);
+                    if ((unsigned)pg >= (unsigned)p.num_pages) {
+                        record_status(p.status, PKV_ERR_DEVICE_BOUNDS);
+                        return -1;
+                    }
+                    return pg;
+                };
+                int pg = load_id(0);
+                for (int j = 0; okp && j < n_tiles; ++j) {
+                    const int j0 = prefill_kv_key_at(it, j, T);
+                    const int slot0 = P > T ? j0 % P : 0;
+                    int pg_next = -1;
+                    // K, then V. Both complete the K slot's barrier; a V tile reaching
+                    // past the cache end lands on the producer's own barrier instead:
+                    // its rows past the end hold stale or foreign data and are zeroed
+                    // (so that P = 0 never meets a non-finite value) before the
+                    // producer's arrival completes the K slot's barrier.
+                    const bool tail = j0 + T > rq.kv_len;
+                    const unsigned valid = __ballot_sync(0xffffffffu, pg >= 0);
+                    const uint32_t bytes = (uint32_t)__popc(valid) * rows_box * Tr::kChunk * NCH;
+                    const uint32_t full = bar(B::kFull + n % NS);
+                    for (int isv = 0; isv < 2; ++isv, ++n) {
+                        const int s = n % NS;
+                        if (n >= NS) {
+                            okp = __all_sync(0xffffffffu, mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v,
+                                                                    kWaitLimitPP));
+                            if (!okp)
+                                break;
+                        }
+                        const bool vtail = isv == 1 && tail;
+                        const uint32_t land = vtail ? bar(B::kVLand) : full;
+                        if (lane == 0) {
+                            if (isv == 0 && tail)
+                                mbar_expect_tx(full, bytes);  // the arrival comes after the zeroing
+                            else if (isv == 0)
+                                mbar_arrive_expect_tx(full, 2 * bytes);
+                            else if (vtail)
+                                mbar_arrive_expect_tx(land, bytes);
+                        }
+                        __syncwarp();
+                        if (pg >= 0) {
+                            const void *tm = isv ? (const void *)&tm_v : (const void *)&tm_k;
+                            for (int c = 0; c < NCH; ++c)
+                                tma_load_4d(slot(s) + c * (T * Tr::kChunk) + lane * rows_box * Tr::kChunk, tm,
+                                            c * 64, it.kv_head, slot0, pg, land);
+                        }
+                        if (isv == 0 && j + 1 < n_tiles)
+                            pg_next = load_id(j + 1);
+                        if (vtail) {
+                            okp = __all_sync(0xffffffffu,
+                                             mbar_wait(bar(B::kVLand), n_land & 1, abort_v, kWaitLimitPP));
+                            ++n_land;
+                            if (!okp)
+                                break;
+                            const int vr = max(0, rq.kv_len - j0);
+                            const int n16 = (T - vr) * 8;  // 16-byte granules per chunk
+                            for (int idx = lane; idx < n16 * NCH; idx += 32) {
+                                const int c = idx / n16, e = idx % n16;
+                                const uint32_t a = slot(s) + c * (T * Tr::kChunk) + (vr + e / 8) * Tr::kChunk + (e % 8) * 16;
+                                asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(a), "r"(0) : "memory");
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(full);
+                        }
+                    }
+                    pg = pg_next;
+                }
+            }
+            if (!okp && lane == 0) {
+                record_status(p.status, PKV_ERR_TIMEOUT);
+                abort_flag = 1;
+            }
+        }
+    } else if (!KV8) {
+        // ------------------------------------------------------------ cp.async producers
+        constexpr int NP = Tr::kProducers;
+        const int pt = threadIdx.x - 9 * 32;
+        // Work unit = one row and 8 consecutive 16-byte chunks (one 128-byte
+        // plane row): one page-table lookup feeds 8 copies. Rows past the cache end
+        // are zero-filled. The page id of every row is fetched kIdRing - 1 tiles
+        // ahead into the shared ring by cp.async (the producers never stall on a
+        // page-table read); named barrier 1 orders the ring among the producers.
+        constexpr int kUnits = T * (CH / 8);
+        int c_ii = item_lo, c_j = 0, c_at = -1;
+        PrefillItem c_it{};
+        int c_kv_len = 0, c_page_begin = 0;
+        uint32_t n_ids = 0;
+        auto fetch_ids = [&]() {
+            while (c_ii < item_hi) {
+                if (c_at != c_ii) {
+                    c_it = p.items[c_ii];
+                    const RequestInfo r = p.reqs[c_it.req];
+                    c_kv_len = r.kv_len;
+                    c_page_begin = r.kv_page_begin;
+                    c_at = c_ii;
+                }
+                if (c_j < c_it.kv_tiles)
+                    break;
+                ++c_ii;
+                c_j = 0;
+            }
+            if (c_ii < item_hi) {
+                const int j0 = prefill_kv_key_at(c_it, c_j, T);
+                for (int t = pt; t < T; t += NP) {
+                    int *dst = &id_ring[(n_ids % kIdRing) * Tr::kIdsPerTile + t];
+                    const int jj = j0 + t;
+                    if (jj < c_kv_len) {
+                        const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
+                        cp_async_4(smem_u32(dst), p.kv_indices + c_page_begin + lp);
+                    } else {
+                        *dst = -1;
+                    }
+                }
+            }
+            cp_async_commit();
+            ++c_j;
+            ++n_ids;
+        };
+        auto sync_producers = [] { asm volatile("bar.sync 1, %0;\n" ::"n"(Tr::kProducers) : "memory"); };
+        for (int k = 0; k < kIdRing - 1; ++k)
+            fetch_ids();
+        uint32_t n = 0;    // K/V ring position
+        uint32_t n_t = 0;  // tiles gathered so far
+        bool okp = true;
+        for (int ii = item_lo; okp && ii < item_hi; ++ii) {
+            const PrefillItem it = p.items[ii];
+            const int n_tiles = it.kv_tiles;
+            if (n_tiles <= 0)
+                continue;
+            for (int j = 0; okp && j < n_tiles; ++j, ++n_t) {
+                const int j0 = prefill_kv_key_at(it, j, T);
+                sync_producers();  // every producer is done with the ring entry refilled next
+                fetch_ids();
+                cp_async_wait<kIdRing - 1>();
+                sync_producers();  // this tile's ids are visible to all producers
+                const int *ids = &id_ring[(n_t % kIdRing) * Tr::kIdsPerTile];
+                const uint32_t full = bar(B::kFull + n % NS);  // K and V of the tile complete it
+                for (int isv = 0; isv < 2; ++isv, ++n) {
+                    const int s = n % NS;
+                    if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP)) {
+                        okp = false;
+                        break;
+                    }
+                    const uint16_t *src = isv ? p.v_cache : p.k_cache;
+                    for (int u = pt; u < kUnits; u += NP) {
+                        const int t = u / (CH / 8), pl = u % (CH / 8);  // row, 64-column plane
+                        const int jj = j0 + t;
+                        const int page = ids[t];
+                        size_t off = 0;
+                        uint32_t bytes = 0;
+                        if (page >= 0) {
+                            if ((unsigned)page < (unsigned)p.num_pages) {
+                                const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
+                                const int sl = jj - lp * p.page_size;
+                                off = (((size_t)page * p.page_size + sl) * p.num_kv_heads + it.kv_head) * D + pl * 64;
+                                bytes = 16;
+                            } else {
+                                record_status(p.status, PKV_ERR_DEVICE_BOUNDS);
+                            }
+                        }
+                        const uint32_t row_base = slot(s) + pl * (T * Tr::kChunk) + t * Tr::kChunk;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            cp_async_16(row_base + ((c ^ (t & 7)) << 4), src + off + c * 8, bytes);
+                    }
+                    if (isv == 1)
+                        cp_async_mbar_arrive(full);
+                }
+            }
+        }
+        if (!okp) {
+            record_status(p.status, PKV_ERR_TIMEOUT);
+            abort_flag = 1;
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+    } else {
+        // ------------------------------------------------------------ 8-bit K/V producers
+        // Round n: the 8-bit K and V rows of this CTA's n-th KV tile are copied by
+        // cp.async into staging buffer n % 2 (rows past the cache end or behind a bad
+        // page id are zero-filled), while the tile staged in round n - 1 is widened to
+        // f16 into its ring slots, in the layout the TMA path produces. Each thread's
+        // page ids for the next tile are loaded one round ahead.
+        constexpr int NP = Tr::kProducers;
+        constexpr bool E5 = KV == PKV_FP8_E5M2;
+        constexpr int CPR = D / 16;                   // 16-byte chunks per 8-bit row
+        constexpr int SWZ = (CPR < 8 ? CPR : 8) - 1;  // chunk swizzle of the staging rows
+        constexpr int kUPT = (2 * T + NP - 1) / NP;   // copy units (row, K or V) per thread
+        const int pt = threadIdx.x - 9 * 32;
+        const uint8_t *kc = reinterpret_cast<const uint8_t *>(p.k_cache);
+        const uint8_t *vc = reinterpret_cast<const uint8_t *>(p.v_cache);
+        auto sync_producers = [] { asm volatile("bar.sync 1, %0;\n" ::"n"(NP) : "memory"); };
+        auto first_from = [&](int ii) {
+            while (ii < item_hi && p.items[ii].kv_tiles <= 0)
+                ++ii;
+            return ii;
+        };
+        // Page id (-1: no key) and slot of each of this thread's copy units of tile (ii, j).
+        auto load_ids = [&](int ii, int j, int (&pg)[kUPT], int (&sl)[kUPT]) {
+            const PrefillItem it = p.items[ii];
+            const RequestInfo rq = p.reqs[it.req];
+            const int j0 = prefill_kv_key_at(it, j, T);
+#pragma unroll
+            for (int k = 0; k < kUPT; ++k) {
+                const int u = pt + k * NP;
+                const int jj = j0 + u % T;
+                pg[k] = -1;
+                sl[k] = 0;
+                if (u < 2 * T && jj < rq.kv_len) {
+                    const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
+                    pg[k] = __ldg(p.kv_indices + rq.kv_page_begin + lp);
+                    sl[k] = jj - lp * p.page_size;
+                }
+            }
+        };
+        int cur_ii = first_from(item_lo), cur_j = 0;
+        int pg[kUPT], sl[kUPT];
+        if (cur_ii < item_hi)
+            load_ids(cur_ii, cur_j, pg, sl);
+        uint32_t n = 0;  // ring position of the next tile to widen (K at n, V at n + 1)
+        int staged = 0;  // tiles copied so far
+        bool okp = true;
+        while (true) {
+            const bool have = cur_ii < item_hi;
+            sync_producers();  // buffer staged % 2 was widened last round by every producer
+            if (have) {
+                const uint32_t stg = sStg + (uint32_t)(staged & 1) * Tr::kStgTileBytes;
+                const int kvh = p.items[cur_ii].kv_head;
+#pragma unroll
+                for (int k = 0; k < kUPT; ++k) {
+                    const int u = pt + k * NP;
+                    if (u >= 2 * T)
+                        continue;
+                    const int t = u % T, isv = u / T;
+                    int64_t off = -1;
+                    if (pg[k] >= 0) {
+                        if ((unsigned)pg[k] < (unsigned)p.num_pages)
+                            off = (((int64_t)pg[k] * p.page_size + sl[k]) * p.num_kv_heads + kvh) * D;
+                        else
+                            record_status(p.status, PKV_ERR_DEVICE_BOUNDS);
+                    }
+                    const uint8_t *src = (isv ? vc : kc) + (off >= 0 ? off : 0);
+                    const uint32_t bytes = off >= 0 ? 16u : 0u;
+                    const uint32_t drow = stg + (uint32_t)(isv * T * D + t * D);
+#pragma unroll
+                    for (int c = 0; c < CPR; ++c)
+                        cp_async_16(drow + ((c ^ (t & SWZ)) << 4), src + c * 16, bytes);
+                }
+            }
+            cp_async_commit();
+            // The next tile, and its page ids (in flight until the next round).
+            int nii = cur_ii, nj = cur_j;
+            if (have && ++nj >= p.items[nii].kv_tiles) {
+                nii = first_from(nii + 1);
+                nj = 0;
+            }
+            int npg[kUPT], nsl[kUPT];
+            if (nii < item_hi)
+                load_ids(nii, nj, npg, nsl);
+            if (staged > 0) {
+                cp_async_wait<1>();
+                sync_producers();  // the previous tile's rows have landed for every producer
+                const uint32_t stg = sStg + (uint32_t)((staged - 1) & 1) * Tr::kStgTileBytes;
+                for (int isv = 0; isv < 2; ++isv) {
+                    const uint32_t pos = n + isv;
+                    const int s = pos % NS;
+                    const bool w_ok =
+                        pos < NS || mbar_wait(bar(B::kEmpty + s), ((pos / NS) - 1) & 1, abort_v, kWaitLimitPP);
+                    okp = bar_red_and(1, NP, w_ok);  // every producer takes the same way out
+                    if (!okp)
+                        break;
+                    const uint32_t src0 = stg + (uint32_t)(isv * T * D), dst0 = slot(s);
+                    for (int u = pt; u < T * CPR; u += NP) {
+                        const int t = u / CPR, c = u % CPR;
+                        uint32_t w0, w1, w2, w3;
+                        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                                     : "r"(src0 + (uint32_t)(t * D) + ((c ^ (t & SWZ)) << 4))
+                                     : "memory");
+                        uint32_t f[8];
+                        fp8x4_widen_f16<E5>(w0, f[0], f[1]);
+                        fp8x4_widen_f16<E5>(w1, f[2], f[3]);
+                        fp8x4_widen_f16<E5>(w2, f[4], f[5]);
+                        fp8x4_widen_f16<E5>(w3, f[6], f[7]);
+                        // columns 16c .. 16c+15 = granules 2(c % 4), 2(c % 4) + 1 of plane c / 4
+                        const int k0 = (c & 3) * 2;
+                        const uint32_t row = dst0 + (uint32_t)((c >> 2) * (T * Tr::kChunk) + t * Tr::kChunk);
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(row + ((k0 ^ (t & 7)) << 4)),
+                                     "r"(f[0]), "r"(f[1]), "r"(f[2]), "r"(f[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(
+                                         row + (((k0 + 1) ^ (t & 7)) << 4)),
+                                     "r"(f[4]), "r"(f[5]), "r"(f[6]), "r"(f[7])
+                                     : "memory");
+                    }
+                }
+                if (!okp)
+                    break;
+                fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
+                mbar_arrive(bar(B::kFull + n % NS));
+                n += 2;
+            }
+            if (!have)
+                break;
+            ++staged;
+            cur_ii = nii;
+            cur_j = nj;
+#pragma unroll
+            for (int k = 0; k < kUPT; ++k) {
+                pg[k] = npg[k];
+                sl[k] = nsl[k];
+            }
+        }
+        if (!okp) {
+            record_status(p.status, PKV_ERR_TIMEOUT);
+            abort_flag = 1;
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Tr::kTmemCols);
+    }
+}
+
+template <int D, int MASK, bool TMA_KV, bool RAGGED, int KV>
+cudaError_t launch_pp_dmt(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tv, int num_ctas, cudaStream_t s)
+{
+    using Tr = PPTraits<D, KV != PKV_BF16>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_pp_kernel<D, MASK, TMA_KV, RAGGED, KV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kDynSmem);
+        if (e != cudaSuccess)
+            return e;
+        configured = true;
+    }
+    prefill_pp_kernel<D, MASK, TMA_KV, RAGGED, KV><<<num_ctas, Tr::kThreads, Tr::kDynSmem, s>>>(p, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+template <int D, bool TMA_KV, bool RAGGED, int KV>
+cudaError_t launch_pp_dt(const PrefillParams &p, int mask_mode, const CUtensorMap &tq, const CUtensorMap &tk,
+                         const CUtensorMap &tv, int num_ctas, cudaStream_t s)
+{
+    switch (mask_mode) {
+    case kMaskNone: return launch_pp_dmt<D, kMaskNone, TMA_KV, RAGGED, KV>(p, tq, tk, tv, num_ctas, s);
+    case kMaskCausal: return launch_pp_dmt<D, kMaskCausal, TMA_KV, RAGGED, KV>(p, tq, tk, tv, num_ctas, s);
+    case kMaskCausalWindow:
+        return launch_pp_dmt<D, kMaskCausalWindow, TMA_KV, RAGGED, KV>(p, tq, tk, tv, num_ctas, s);
+    case kMaskWindow: return launch_pp_dmt<D, kMaskWindow, TMA_KV, RAGGED, KV>(p, tq, tk, tv, num_ctas, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pp
+}  // namespace pkv

@@ -133,6 +133,35 @@ __device__ __forceinline__ float soft_cap_tanh(float y)
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
+// Named barrier `id` over n threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool bar_red_and(int id, int n, bool pred)
+{
+    int r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+                 " selp.s32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r)
+                 : "r"((int)pred), "r"(id), "r"(n)
+                 : "memory");
+    return r != 0;
+}
+
+// Four 8-bit values (a 32-bit word, lowest byte first) as two f16x2 words {x0, x1},
+// {x2, x3}: E4M3 through the conversion instruction, E5M2 by byte moves (an E5M2
+// byte is the top byte of its f16). Every value of either format is exact in f16.
+template <bool E5M2>
+__device__ __forceinline__ void fp8x4_widen_f16(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    if (E5M2) {
+        lo = __byte_perm(w, 0u, 0x1404);
+        hi = __byte_perm(w, 0u, 0x3424);
+    } else {
+        asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
+            " cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+    }
+}
+
 __device__ __forceinline__ void record_status(int32_t *status, int32_t code)
 {
     atomicCAS(status, 0, code);

@@ -194,7 +194,7 @@ class Plan:
         capacity={"max_batch": B, "max_total_q": Q}: a capturable plan (its run may
         be captured in a CUDA graph and replayed after update()).
         kv_dtype: element type of the caches, "bf16", "e4m3" or "e5m2" (or the torch
-        dtype); the 8-bit ones are for decode plans."""
+        dtype); the 8-bit ones are for paged (decode and prefill) plans."""
         self._lib = load_library()
         self._handle = ctypes.c_void_p()
         self.kind = kind

@@ -95,8 +95,7 @@ def _desc(**over):
     (dict(num_qo_heads=258, num_kv_heads=2), pkv.PKV_ERR_UNSUPPORTED),
     (dict(kv_dtype=1), pkv.PKV_ERR_INVALID_ARG),
     (dict(kv_dtype=4), pkv.PKV_ERR_INVALID_ARG),
-    (dict(kv_dtype=pkv.PKV_FP8_E4M3), pkv.PKV_ERR_UNSUPPORTED),  # 8-bit caches: decode plans only
-    (dict(kv_dtype=pkv.PKV_FP8_E5M2, kind=pkv.PKV_PREFILL_RAGGED), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(kv_dtype=pkv.PKV_FP8_E5M2, kind=pkv.PKV_PREFILL_RAGGED), pkv.PKV_ERR_UNSUPPORTED),  # paged only
 ])
 def test_plan_rejects_bad_arguments(lib, over, status):
     d, keep = _desc(**over)

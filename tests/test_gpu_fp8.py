@@ -1,6 +1,7 @@
-"""8-bit K/V caches (E4M3, E5M2) in decode: the CUDA path through the C ABI against
-the float64 oracle, which decodes every byte from the format's definition. Same
-bar as the bf16 path: max |diff| <= 2e-2 on out, <= 1e-3 on lse, empty rows exact."""
+"""8-bit K/V caches (E4M3, E5M2) in decode and prefill: the CUDA path through the C
+ABI against the float64 oracle, which decodes every byte from the format's
+definition. Same bar as the bf16 path: max |diff| <= 2e-2 on out, <= 1e-3 on lse,
+empty rows exact."""
 from __future__ import annotations
 
 import numpy as np
@@ -193,3 +194,83 @@ def test_fp8_long_decode_sampled(pkv, oracle_lib, fmt):
                   what=f"long decode {fmt}")
     del w, out, lse
     torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def _prefill(d, W, P, seed, heads=(8, 2), causal=True):
+    return wl.make_workload(name="pf8", qo_lens=[70, 1, 300, 0, 129], kv_lens=[70, 200, 333, 5, 700],
+                            num_qo_heads=heads[0], num_kv_heads=heads[1], head_dim=d, page_size=P,
+                            window_left=W, causal=causal, seed=seed)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("W", [-1, 0, 31, 500])
+@pytest.mark.parametrize("P", [1, 16])
+def test_fp8_prefill_sweep(pkv, oracle_lib, fmt, d, W, P):
+    """Prefix + extend rows, ragged tails, several query tiles, windows, page sizes."""
+    _check(pkv, oracle_lib, to_kv8(_prefill(d, W, P, seed=d * 1000 + abs(W) + P), fmt))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("group", [1, 3, 8, 16])
+def test_fp8_prefill_gqa(pkv, oracle_lib, fmt, group):
+    """Head groups of 1 to 16 (128 / group query tokens per 128-row tile; 3 leaves
+    unused rows in every tile)."""
+    w = _prefill(128, 100, 4, seed=group + 3, heads=(2 * group, 2))
+    _check(pkv, oracle_lib, to_kv8(w, fmt))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("W", [-1, 40])
+def test_fp8_prefill_non_causal(pkv, oracle_lib, fmt, W):
+    _check(pkv, oracle_lib, to_kv8(_prefill(128, W, 16, seed=77 + abs(W), causal=False), fmt))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_fp8_prefill_scales_and_soft_cap(pkv, oracle_lib, fmt, d):
+    from dataclasses import replace
+    ks, vs = 1.0 / 16, 1.0 / 8
+    base = _prefill(d, 100, 16, seed=d + 5)
+    w = replace(to_kv8(base, fmt), k_cache=(base.k_cache.float() / ks).to(wl.KV8_DTYPES[fmt]),
+                v_cache=(base.v_cache.float() / vs).to(wl.KV8_DTYPES[fmt]))
+    kw = dict(logits_soft_cap=6.0, k_scale=ks, v_scale=vs)
+    out, lse, _ = _run(pkv, w, **kw)
+    ref_out, ref_lse = run_oracle(oracle_lib, w, **kw)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"fp8 prefill scales {fmt} d={d}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("qmag", [1e5, 1e-6])
+def test_fp8_prefill_query_range(pkv, oracle_lib, fmt, qmag):
+    """Queries far outside f16's range, sm_scale rescaled: the per-row power-of-two
+    scaling of Q must keep the f16 products exact."""
+    from dataclasses import replace
+    base = _prefill(128, 300, 16, seed=int(qmag > 1) + 60)
+    w = replace(to_kv8(base, fmt), q=(base.q.float() * qmag).to(torch.bfloat16), sm_scale=base.sm_scale / qmag)
+    _check(pkv, oracle_lib, w)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fp8_prefill_many_items(pkv, oracle_lib, fmt):
+    """More work items than CTAs (several per persistent CTA, Q written per item),
+    items with and without KV tiles, both query tiles."""
+    rng = np.random.default_rng(17)
+    qo = rng.integers(0, 300, size=60)
+    kv = qo + rng.integers(0, 400, size=60)
+    w = wl.make_workload(name="pf8many", qo_lens=qo, kv_lens=kv, num_qo_heads=16, num_kv_heads=4, head_dim=128,
+                         page_size=16, window_left=63, causal=True, seed=18, layout_rng=rng)
+    _check(pkv, oracle_lib, to_kv8(w, fmt))
+
+
+def test_fp8_extend_with_prefix_sampled(pkv, oracle_lib):
+    """The extend-with-prefix workload (16 requests, prefix U[0, 8192], extend
+    U[128, 2048], 32/8 heads, d 128, page 16, W 4095) over an E4M3 cache; 512 rows
+    sampled across every request are checked against the oracle."""
+    w = to_kv8(wl.extend_with_prefix(), "e4m3")
+    out, lse, _ = _run(pkv, w)
+    rows = np.sort(np.random.default_rng(9).choice(w.q.shape[0], size=512, replace=False))
+    ref_out, ref_lse = run_oracle(oracle_lib, w, rows=rows)
+    assert_parity(out[rows], lse[rows], ref_out, ref_lse, what="fp8 extend sampled")
