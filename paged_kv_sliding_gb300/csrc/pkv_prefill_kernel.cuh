@@ -892,8 +892,12 @@ __global__ void __launch_bounds__(384, 1)
                     if (!okp)
                         break;
                     const uint32_t src0 = stg + (uint32_t)(isv * T * D), dst0 = slot(s);
+                    // Consecutive threads take consecutive rows of one chunk column: the
+                    // eight 16-byte accesses of a quarter warp then fall in eight
+                    // different bank groups on both sides (staging and slot swizzles).
+#pragma unroll 4
                     for (int u = pt; u < T * CPR; u += NP) {
-                        const int t = u / CPR, c = u % CPR;
+                        const int t = u % T, c = u / T;
                         uint32_t w0, w1, w2, w3;
                         asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
                                      : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
