@@ -14,11 +14,13 @@ cudaError_t launch_kv(const DecodeParams &p, int head_dim, int num_items, cudaSt
 {
     using dec::launch_decode_dt;
     if (tile == 32) {
+        // the short variant: 64-token stages, two compute warps of two 16-token
+        // sub-blocks each, 4 CTAs per SM (decode_kernel_tile)
         switch (head_dim) {
-        case 64: return tma ? launch_decode_dt<64, true, 32, KV>(p, tk, tv, num_items, s)
-                            : launch_decode_dt<64, false, 32, KV>(p, tk, tv, num_items, s);
-        case 128: return tma ? launch_decode_dt<128, true, 32, KV>(p, tk, tv, num_items, s)
-                             : launch_decode_dt<128, false, 32, KV>(p, tk, tv, num_items, s);
+        case 64: return tma ? launch_decode_dt<64, true, 64, KV, 32>(p, tk, tv, num_items, s)
+                            : launch_decode_dt<64, false, 64, KV, 32>(p, tk, tv, num_items, s);
+        case 128: return tma ? launch_decode_dt<128, true, 64, KV, 32>(p, tk, tv, num_items, s)
+                             : launch_decode_dt<128, false, 64, KV, 32>(p, tk, tv, num_items, s);
         default: return cudaErrorInvalidValue;
         }
     }

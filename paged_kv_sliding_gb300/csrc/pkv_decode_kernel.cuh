@@ -55,12 +55,14 @@ struct DecTraits {
     static constexpr int kTileBytes = kTile * kRowBytes;  // K or V of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
     // Stages: about the same bytes in flight per SM for every variant.
-    static constexpr int kStages = TT == 128 ? 3 : (D == 64 ? 4 : 3) * (kElem == 1 ? 2 : 1);
+    static constexpr int kStages =
+        (TT == 128 || (TT == 64 && TPW == 32)) ? 3 : (D == 64 ? 4 : 3) * (kElem == 1 ? 2 : 1);
     static constexpr int kORowFloats = D + 8;  // padded row of the combine buffer
     static constexpr int kCombineBytes = kCompute * kDecodeRows * kORowFloats * 4;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kDynSmem = (kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes) + 1024;
-    static constexpr int kMinBlocks = TT == 32 ? 4 : (D >= 256 ? 1 : 2);
+    // two compute warps (96 threads): 4 CTAs per SM, so a batch of short ranges runs in one wave
+    static constexpr int kMinBlocks = kCompute == 2 ? 4 : (D >= 256 ? 1 : 2);
 };
 
 constexpr long long kDecWaitLimit = 4000000000LL;

@@ -180,11 +180,12 @@ inline int decode_tile_for(int head_dim, int64_t max_keys, int64_t n_items, int 
     return 64;
 }
 // KV tokens per stage of the decode kernel that runs a plan's tile variant (32: short
-// key ranges; 64: the rest): 8-bit caches at head_dim <= 128 run the long variant with
-// 128-token stages, two 16-token sub-blocks per compute warp.
+// key ranges; 64: the rest): 8-bit caches at head_dim <= 128 run both variants with
+// two 16-token sub-blocks per compute warp, so their stages are twice as long (64 and
+// 128 tokens).
 inline int decode_kernel_tile(int tile, int head_dim, int kv_dtype)
 {
-    return (tile == 64 && kv_dtype != PKV_BF16 && head_dim <= 128) ? 128 : tile;
+    return (kv_dtype != PKV_BF16 && head_dim <= 128) ? 2 * tile : tile;
 }
 // Page sizes whose pages the decode kernel loads with TMA boxes of a `tile`-token stage.
 bool decode_tma_page_size(int page_size, int tile);
