@@ -8,7 +8,9 @@ requests with kv_len ~ U[256, 4096], 32 query / 8 KV heads, head_dim 128, page 1
 once for each window_left in {-1, 0, 31, 127, 1023} (plans made beforehand; each
 run = one decode kernel, which also merges split-KV partials when a plan splits). The metric is the algorithmic KV
 bytes read (visible rows x 2 x H_kv x d x 2 B) per second. The line also carries
-the prefill (TFLOP/s) and long-context decode (GB/s) workloads under "workloads".
+the prefill (TFLOP/s) and long-context decode (GB/s) workloads under "workloads",
+including the extend prefill and both decodes over 8-bit (E4M3) K/V caches, whose
+GB/s count one byte per cached element.
 
 L2 is flushed between timed steps, outside the timed events: a 512 MiB write, then a
 256 MiB read of the same buffer (so the flush leaves no dirty line to write back).
