@@ -490,7 +490,10 @@ __global__ void __launch_bounds__(384, 1)
                     const uint32_t nK = n_kv, nV = n_kv + 1;
                     n_kv += 2;
                     const int sK = nK % NS, sV = nV % NS;
-                    if (!(ok = wait(B::kFull + sK, (nK / kFullPeriod) & 1)))
+                    // 8-bit caches: K and V complete their own slots' barriers (one phase
+                    // per use), so S_0 starts as soon as K is widened, V is waited for
+                    // before its first P V.
+                    if (!(ok = wait(B::kFull + sK, (nK / (KV8 ? NS : kFullPeriod)) & 1)))
                         break;
                     if (!TMA_KV)
                         fence_proxy_async_smem();
@@ -517,6 +520,12 @@ __global__ void __launch_bounds__(384, 1)
                     // every read of Q is done and the next item's Q may land.
                     if (!KV8 && nq == 1 && j == n_tiles - 1 && ii_next < item_hi)
                         load_q(ii_next);
+                    if (KV8) {
+                        if (!(ok = wait(B::kFull + sV, (nV / NS) & 1)))
+                            break;
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+                    }
                     issue_pv(0, slot(sV), j == 0);
                     if (nq == 1)
                         umma_commit(bar(B::kEmpty + sV));
@@ -760,10 +769,11 @@ __global__ void __launch_bounds__(384, 1)
                 const uint32_t full = bar(B::kFull + n % NS);  // K and V of the tile complete it
                 for (int isv = 0; isv < 2; ++isv, ++n) {
                     const int s = n % NS;
-                    if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP)) {
-                        okp = false;
+                    const bool w_ok =
+                        n < NS || mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP);
+                    okp = bar_red_and(1, NP, w_ok);  // every producer takes the same way out
+                    if (!okp)
                         break;
-                    }
                     const uint16_t *src = isv ? p.v_cache : p.k_cache;
                     for (int u = pt; u < kUnits; u += NP) {
                         const int t = u / (CH / 8), pl = u % (CH / 8);  // row, 64-column plane
@@ -883,6 +893,7 @@ __global__ void __launch_bounds__(384, 1)
                 cp_async_wait<1>();
                 sync_producers();  // the previous tile's rows have landed for every producer
                 const uint32_t stg = sStg + (uint32_t)((staged - 1) & 1) * Tr::kStgTileBytes;
+                // K, then V, each into its slot and completing that slot's barrier.
                 for (int isv = 0; isv < 2; ++isv) {
                     const uint32_t pos = n + isv;
                     const int s = pos % NS;
@@ -919,11 +930,11 @@ __global__ void __launch_bounds__(384, 1)
                                      "r"(f[4]), "r"(f[5]), "r"(f[6]), "r"(f[7])
                                      : "memory");
                     }
+                    fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
+                    mbar_arrive(bar(B::kFull + s));
                 }
                 if (!okp)
                     break;
-                fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
-                mbar_arrive(bar(B::kFull + n % NS));
                 n += 2;
             }
             if (!have)
