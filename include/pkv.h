@@ -153,7 +153,8 @@ typedef struct pkv_plan_info {
     int64_t workspace_bytes;   /* device memory owned by the plan */
     int64_t total_q;           /* query rows */
     int32_t kernels_per_run;   /* launches issued by one pkv_run */
-    int32_t kv_tile;           /* KV tokens per tile of the main kernel (decode: 32 or 64;
+    int32_t kv_tile;           /* KV tokens per tile of the main kernel (decode: 32 or 64,
+                                  64 or 128 over an 8-bit cache at head_dim <= 128;
                                   prefill: 128, or 64 at head_dim 256) */
 } pkv_plan_info;
 

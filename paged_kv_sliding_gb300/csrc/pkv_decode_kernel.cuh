@@ -6,23 +6,26 @@
 // The plan has already clipped each CTA's key range [j0, j1) to the visible
 // interval [p - W, p] of the request's single query position, so every key inside
 // the range is visible; the kernel masks only what lies outside it in the first
-// and last 64-token tile.
+// and last stage.
 //
-// CTA = TT/16 compute warps + 1 producer warp, TT = 64 tokens per stage (160
-// threads) or, for batches of short key ranges, 32 (96 threads, 4 CTAs per SM):
+// CTA = TT/TPW compute warps + 1 producer warp. bf16 caches: TT = 64 tokens per stage
+// (160 threads, 2 CTAs per SM) or, for batches of short key ranges, 32 (96 threads,
+// 4 CTAs per SM), TPW = 16 tokens per compute warp. 8-bit caches (E4M3 / E5M2): the
+// same two CTA shapes with stages of 128 and 64 tokens, TPW = 32 (two independent
+// 16-token sub-blocks per warp), K and V widened to f16 in registers before the MMAs.
 //   producer: fills a ring of shared-memory stages (TT tokens of K and of V each,
-//     stored as 128-byte-swizzled 64-column planes) either with TMA boxes of whole
-//     pages (a 4-D tensor map over [page, slot, KV head, d]; the page ids of the
-//     next tile are fetched while the current one is issued) when the page size
-//     is a multiple of 8 that divides TT or is a multiple of it, or else with
-//     16-byte cp.async gathers; completion through mbarriers;
-//   compute warp w: tokens [16w, 16w + 16) of every tile, S = Q K^T and O += P V
-//     with mma.sync m16n8k16 (bf16 in, fp32 accumulate, rows = the query heads),
-//     running its own (m, l, O) without CTA-wide barriers; the four states are
-//     merged once at the end. A CTA that handles one split of a request writes an
-//     fp32 partial state; the group's last CTA to finish (an arrival counter after
-//     a memory fence) combines the partials through their LSE, so no second
-//     kernel runs.
+//     stored as 128-byte-swizzled planes) either with TMA boxes of whole pages (a
+//     4-D tensor map over [page, slot, KV head, d]; the page ids of the next tile
+//     are fetched while the current one is issued) when the page size is a multiple
+//     of 8 that divides TT or is a multiple of it, or else with 16-byte cp.async
+//     gathers; completion through mbarriers;
+//   compute warp w: tokens [TPW w, TPW w + TPW) of every stage, S = Q K^T and
+//     O += P V with mma.sync m16n8k16 (bf16, or f16 for 8-bit caches, in; fp32
+//     accumulate; rows = the query heads), running its own (m, l, O) without
+//     CTA-wide barriers; the warps' states are merged once at the end. A CTA that
+//     handles one split of a request writes an fp32 partial state; the group's
+//     last CTA to finish (an arrival counter after a memory fence) combines the
+//     partials through their LSE, so no second kernel runs.
 // All waits are bounded; on expiry PKV_ERR_TIMEOUT is recorded and the CTA winds
 // down after its outstanding copies have landed.
 #pragma once
