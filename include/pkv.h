@@ -264,7 +264,8 @@ PKV_API int pkv_plan_set_timing_events(pkv_plan *plan, void *ev_begin, void *ev_
 
 /*
  * pkv_decode_noalloc: the decode of pkv_plan_create + pkv_run (desc->kind must be
- * PKV_DECODE; same arguments, layouts and results) in one call that allocates no
+ * PKV_DECODE, desc->kv_dtype PKV_BF16, else PKV_ERR_UNSUPPORTED; same arguments,
+ * layouts and results) in one call that allocates no
  * device memory: no cudaMalloc, cudaFree or allocating library routine. The pages
  * have no counterpart to it. It is for callers that cannot allocate: serving
  * processes whose memory pool already holds the device memory and forbids further

@@ -86,6 +86,8 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
         return noalloc_fail(PKV_ERR_UNSUPPORTED, "head_dim not in {64, 128, 256}");
     if (d->page_size <= 0 || d->num_pages < 0 || d->dtype != PKV_BF16)
         return noalloc_fail(PKV_ERR_INVALID_ARG, "page_size, num_pages or dtype");
+    if (d->kv_dtype != PKV_BF16)
+        return noalloc_fail(PKV_ERR_UNSUPPORTED, "bf16 caches only (kv_dtype must be PKV_BF16)");
     for (float x : {d->logits_soft_cap, d->k_scale, d->v_scale})
         if (!(x == x) || std::isinf(x))
             return noalloc_fail(PKV_ERR_INVALID_ARG, "logits_soft_cap, k_scale and v_scale must be finite");

@@ -123,6 +123,18 @@ def test_null_arguments(lib):
     assert lib.pkv_plan_set_timing_events(None, None, None) == pkv.PKV_ERR_INVALID_ARG
 
 
+def test_noalloc_decode_rejects_8bit_caches_on_the_host(lib):
+    """The allocation-free decode reads bf16 caches only: an 8-bit kv_dtype is refused
+    before any device work (it would otherwise read the bytes as bf16)."""
+    d, keep = _desc(kind=pkv.PKV_DECODE, qo_indptr=np.array([0, 1, 2], dtype=np.int32),
+                    kv_dtype=pkv.PKV_FP8_E4M3)
+    d.qo_indptr = None
+    rc = lib.pkv_decode_noalloc(ctypes.byref(d), ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000),
+                                ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000), None, None)
+    assert rc == pkv.PKV_ERR_UNSUPPORTED, lib.pkv_last_error()
+    assert "kv_dtype" in lib.pkv_last_error().decode()
+
+
 def test_merge_state_rejects_bad_arguments(lib):
     p = ctypes.c_void_p(0x1000)
     assert lib.pkv_merge_state(p, p, p, p, p, p, 4, 2, 128, 5, None) == pkv.PKV_ERR_UNSUPPORTED
