@@ -808,11 +808,11 @@ __global__ void __launch_bounds__(384, 1)
         asm volatile("cp.async.wait_all;\n" ::: "memory");
     } else {
         // ------------------------------------------------------------ 8-bit K/V producers
-        // Round n: the 8-bit K and V rows of this CTA's n-th KV tile are copied by
+        // Step n: the 8-bit K and V rows of this CTA's n-th KV tile are copied by
         // cp.async into staging buffer n % 2 (rows past the cache end or behind a bad
-        // page id are zero-filled), while the tile staged in round n - 1 is widened to
+        // page id are zero-filled), while the tile staged in step n - 1 is widened to
         // f16 into its ring slots, in the layout the TMA path produces. Each thread's
-        // page ids for the next tile are loaded one round ahead.
+        // page ids for the next tile are loaded one step ahead.
         constexpr int NP = Tr::kProducers;
         constexpr bool E5 = KV == PKV_FP8_E5M2;
         constexpr int CPR = D / 16;                   // 16-byte chunks per 8-bit row
@@ -854,7 +854,7 @@ __global__ void __launch_bounds__(384, 1)
         bool okp = true;
         while (true) {
             const bool have = cur_ii < item_hi;
-            sync_producers();  // buffer staged % 2 was widened last round by every producer
+            sync_producers();  // buffer staged % 2 was widened in the previous step by every producer
             if (have) {
                 const uint32_t stg = sStg + (uint32_t)(staged & 1) * Tr::kStgTileBytes;
                 const int kvh = p.items[cur_ii].kv_head;
@@ -880,7 +880,7 @@ __global__ void __launch_bounds__(384, 1)
                 }
             }
             cp_async_commit();
-            // The next tile, and its page ids (in flight until the next round).
+            // The next tile, and its page ids (in flight until the next step).
             int nii = cur_ii, nj = cur_j;
             if (have && ++nj >= p.items[nii].kv_tiles) {
                 nii = first_from(nii + 1);
