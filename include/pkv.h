@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 4
+#define PKV_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define PKV_API __attribute__((visibility("default")))
@@ -140,6 +140,20 @@ typedef struct pkv_plan_desc {
      * K = k_scale * (stored value) and V = v_scale * (stored value); q and out stay
      * bf16. PREFILL_RAGGED plans take bf16 K/V only (PKV_ERR_UNSUPPORTED otherwise). */
     int32_t kv_dtype;
+    /* Bound of every wait inside the kernels of this plan's runs, in microseconds;
+     * <= 0 means the default of 2 s. A wait that runs out records PKV_ERR_TIMEOUT in
+     * the plan's device status (pkv_plan_device_status), the kernel's other roles leave
+     * at their next wait, the copies and tensor-core operations already issued are
+     * waited for (each wait again bounded), and the kernel returns: a clear error
+     * instead of a launch that never ends (the failure mode AMD flashinfer PR #234,
+     * "Why each fix", turns into an error at plan time). */
+    int32_t wait_limit_us;
+    /* Test hook for the path above: nonzero makes the first wait of every CTA's
+     * consuming role (decode: the compute warps' first K/V stage; prefill: the
+     * tensor-core issuer's first K/V tile) wait on a barrier that nothing completes,
+     * so that it runs out after wait_limit_us. Out and lse are then unspecified.
+     * Leave 0 in normal use. */
+    int32_t wait_probe;
 } pkv_plan_desc;
 
 typedef struct pkv_plan pkv_plan;
@@ -204,7 +218,7 @@ PKV_API int pkv_plan_create_capturable(pkv_plan **out, const pkv_plan_desc *desc
  * in `desc` (qo_indptr, kv_indptr, kv_last_page_len, q_start, batch_size,
  * fixed_split_size, disable_split_kv) may change; kind, head counts, head_dim,
  * page_size, window_left, causal, sm_scale, dtype, kv_dtype, logits_soft_cap, k_scale,
- * v_scale, num_pages and the kv_indices
+ * v_scale, wait_limit_us, wait_probe, num_pages and the kv_indices
  * device pointer must equal the plan's (the caller rewrites that array's contents,
  * stream-ordered before the next run), else PKV_ERR_INVALID_ARG. A batch above the
  * capacity returns PKV_ERR_UNSUPPORTED and leaves the plan unchanged.
@@ -278,10 +292,14 @@ PKV_API int pkv_plan_set_timing_events(pkv_plan *plan, void *ev_begin, void *ev_
  * is rejected with PKV_ERR_UNSUPPORTED before any launch (pkv_last_error() gives
  * the size; fewer splits, disable_split_kv, or pkv_plan_create + pkv_run handle it).
  * The first call on a device looks up the array's device address (with that device
- * current); make that first call before any stream capture. Every call shares the
- * array: calls whose work overlaps on the GPU (other streams, or other host threads)
- * race and must be serialised by the caller. Out-of-range page ids are skipped as
- * in pkv_run, but this call has no device status to read them back.
+ * current); make that first call before any stream capture. The work list reaches
+ * the array through the arguments of small copy kernels enqueued on `stream` before
+ * the decode, so the host never waits for the stream's earlier work. Every call
+ * shares the array: calls whose work overlaps on the GPU (other streams, or other
+ * host threads) race and must be serialised by the caller. This call has no device
+ * status to read back: out-of-range page ids are skipped as in pkv_run, and a device
+ * wait that gives up (PKV_ERR_TIMEOUT under pkv_run) leaves out and lse incomplete,
+ * both without a report.
  */
 PKV_API int pkv_decode_noalloc(const pkv_plan_desc *desc, const void *q, const void *k_cache,
                                const void *v_cache, void *out, float *lse, void *stream);

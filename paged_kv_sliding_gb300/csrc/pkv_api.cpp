@@ -698,11 +698,12 @@ int pkv_plan_update(pkv_plan *plan, const pkv_plan_desc *desc, void *stream_)
         d.head_dim != o.head_dim || d.page_size != o.page_size || W != o.window_left ||
         (d.causal != 0) != (o.causal != 0) || d.sm_scale != o.sm_scale || d.dtype != o.dtype ||
         d.logits_soft_cap != o.logits_soft_cap || d.k_scale != o.k_scale || d.v_scale != o.v_scale ||
-        d.kv_dtype != o.kv_dtype ||
+        d.kv_dtype != o.kv_dtype || d.wait_limit_us != o.wait_limit_us || d.wait_probe != o.wait_probe ||
         d.num_pages != o.num_pages || d.kv_indices != o.kv_indices)
         return fail(PKV_ERR_INVALID_ARG,
                     "update must keep kind, heads, head_dim, page_size, window_left, causal, sm_scale, "
-                    "dtype, kv_dtype, soft cap, scales, num_pages and the kv_indices pointer of the plan");
+                    "dtype, kv_dtype, soft cap, scales, wait bound and probe, num_pages and the kv_indices "
+                    "pointer of the plan");
     if (d.batch_size > plan->cap_batch)
         return fail(PKV_ERR_UNSUPPORTED, "batch %d exceeds the plan's capacity %lld", d.batch_size,
                     (long long)plan->cap_batch);
@@ -869,6 +870,8 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
         p.cap_out = lf.cap_out;
         p.v_scale = lf.v_scale;
         p.kv_dtype = d.kv_dtype;
+        p.wait_probe = d.wait_probe;
+        p.wait_ns = wait_ns_of(d);
         if (plan->ev_begin && (ce = cudaEventRecord(plan->ev_begin, stream)) != cudaSuccess)
             return cuda_fail(ce, "cudaEventRecord");
         ce = launch_decode(p, d.head_dim, plan->capturable ? (int)plan->cap_items : plan->num_items, stream,
@@ -906,6 +909,8 @@ int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void
     p.v_scale = lf.v_scale;
     p.ragged = d.kind == PKV_PREFILL_RAGGED ? 1 : 0;
     p.kv_dtype = d.kv_dtype;
+    p.wait_probe = d.wait_probe;
+    p.wait_ns = wait_ns_of(d);
     p.total_kv = (int32_t)plan->total_kv;
     if (p.ragged) {
         p.page_size = 1;

@@ -43,7 +43,8 @@ bool decode_tma_page_size(int page_size, int tile)
     return page_size <= tile ? tile % page_size == 0 : page_size % tile == 0;
 }
 
-cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile)
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile,
+                          bool overlap_prev)
 {
     using dec::launch_decode_dt;
     if (tile == 32 && head_dim > 128)
@@ -58,24 +59,24 @@ cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cu
             return cudaErrorInvalidValue;
     }
     if (p.kv_dtype != PKV_BF16)
-        return launch_decode_kv8(p, head_dim, num_items, s, tile, tma, tk, tv);
+        return launch_decode_kv8(p, head_dim, num_items, s, tile, tma, tk, tv, overlap_prev);
     constexpr int BF = PKV_BF16;
     if (tile == 32) {
         switch (head_dim) {
-        case 64: return tma ? launch_decode_dt<64, true, 32, BF>(p, tk, tv, num_items, s)
-                            : launch_decode_dt<64, false, 32, BF>(p, tk, tv, num_items, s);
-        case 128: return tma ? launch_decode_dt<128, true, 32, BF>(p, tk, tv, num_items, s)
-                             : launch_decode_dt<128, false, 32, BF>(p, tk, tv, num_items, s);
+        case 64: return tma ? launch_decode_dt<64, true, 32, BF>(p, tk, tv, num_items, s, overlap_prev)
+                            : launch_decode_dt<64, false, 32, BF>(p, tk, tv, num_items, s, overlap_prev);
+        case 128: return tma ? launch_decode_dt<128, true, 32, BF>(p, tk, tv, num_items, s, overlap_prev)
+                             : launch_decode_dt<128, false, 32, BF>(p, tk, tv, num_items, s, overlap_prev);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (head_dim) {
-    case 64: return tma ? launch_decode_dt<64, true, 64, BF>(p, tk, tv, num_items, s)
-                        : launch_decode_dt<64, false, 64, BF>(p, tk, tv, num_items, s);
-    case 128: return tma ? launch_decode_dt<128, true, 64, BF>(p, tk, tv, num_items, s)
-                         : launch_decode_dt<128, false, 64, BF>(p, tk, tv, num_items, s);
-    case 256: return tma ? launch_decode_dt<256, true, 64, BF>(p, tk, tv, num_items, s)
-                         : launch_decode_dt<256, false, 64, BF>(p, tk, tv, num_items, s);
+    case 64: return tma ? launch_decode_dt<64, true, 64, BF>(p, tk, tv, num_items, s, overlap_prev)
+                        : launch_decode_dt<64, false, 64, BF>(p, tk, tv, num_items, s, overlap_prev);
+    case 128: return tma ? launch_decode_dt<128, true, 64, BF>(p, tk, tv, num_items, s, overlap_prev)
+                         : launch_decode_dt<128, false, 64, BF>(p, tk, tv, num_items, s, overlap_prev);
+    case 256: return tma ? launch_decode_dt<256, true, 64, BF>(p, tk, tv, num_items, s, overlap_prev)
+                         : launch_decode_dt<256, false, 64, BF>(p, tk, tv, num_items, s, overlap_prev);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -26,8 +26,9 @@
 //     handles one split of a request writes an fp32 partial state; the group's
 //     last CTA to finish (an arrival counter after a memory fence) combines the
 //     partials through their LSE, so no second kernel runs.
-// All waits are bounded; on expiry PKV_ERR_TIMEOUT is recorded and the CTA winds
-// down after its outstanding copies have landed.
+// All waits are bounded (the plan's wait bound, 2 s by default); on expiry
+// PKV_ERR_TIMEOUT is recorded and the CTA winds down after its outstanding copies
+// have landed.
 #pragma once
 
 #include <cfloat>
@@ -67,8 +68,6 @@ struct DecTraits {
     // two compute warps (96 threads): 4 CTAs per SM, so a batch of short ranges runs in one wave
     static constexpr int kMinBlocks = kCompute == 2 ? 4 : (D >= 256 ? 1 : 2);
 };
-
-constexpr long long kDecWaitLimit = 4000000000LL;
 
 // Byte offset of 16-byte granule `c16` of row `row` in a TT-row tile stored as
 // planes of PR-byte rows: PR = 128 with the 128-byte XOR swizzle (the layout a
@@ -132,6 +131,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
     __shared__ float red_l[NW][kDecodeRows];
     __shared__ float row_m[kDecodeRows];
     __shared__ float row_inv_l[kDecodeRows];
+    __shared__ __align__(8) uint64_t never_bar;  // the wait probe's barrier: nothing completes it
     __shared__ int abort_flag;
     __shared__ int no_abort;
 
@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
             mbar_init(smem_u32(&full_bar[s]), TMA_KV ? 1 : 32);
             mbar_init(smem_u32(&empty_bar[s]), Tr::kCompute);
         }
+        mbar_init(smem_u32(&never_bar), 1);
         abort_flag = 0;
         no_abort = 0;
         fence_mbarrier_init();
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
                 const int pg_next = t + 1 < ntiles ? load_id(t + 1) : -1;
                 if (t >= S) {
                     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[s]), ((t / S) - 1) & 1, abort_v,
-                                                          kDecWaitLimit));
+                                                          p.wait_ns));
                     if (!ok)
                         break;
                 }
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
                 const int s = t % S;
                 if (t >= S) {
                     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[s]), ((t / S) - 1) & 1, abort_v,
-                                                          kDecWaitLimit));
+                                                          p.wait_ns));
                     if (!ok)
                         break;
                 }
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
         }
         // Never leave with copies in flight: wait for the last stages issued.
         for (int t = issued - S < 0 ? 0 : issued - S; t < issued; ++t)
-            mbar_wait(smem_u32(&full_bar[t % S]), (t / S) & 1, &no_abort, kDecWaitLimit);
+            mbar_wait(smem_u32(&full_bar[t % S]), (t / S) & 1, &no_abort, p.wait_ns);
         if (!TMA_KV)
             asm volatile("cp.async.wait_all;\n" ::: "memory");
     } else {
@@ -350,7 +351,9 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
 
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % S;
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[s]), (t / S) & 1, abort_v, kDecWaitLimit));
+            // (the wait probe replaces the first stage's barrier by one nothing completes)
+            const uint32_t fb = (p.wait_probe && t == 0) ? smem_u32(&never_bar) : smem_u32(&full_bar[s]);
+            ok = __all_sync(0xffffffffu, mbar_wait(fb, (t / S) & 1, abort_v, p.wait_ns));
             if (!ok)
                 break;
             const uint32_t kb = ring + s * Tr::kStageBytes;
@@ -712,7 +715,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
 
 template <int D, bool TMA_KV, int TT, int KV, int TPW = 16>
 cudaError_t launch_decode_dt(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv, int num_items,
-                             cudaStream_t s)
+                             cudaStream_t s, bool overlap_prev)
 {
     using Tr = DecTraits<D, TT, KV, TPW>;
     static bool configured = false;
@@ -723,9 +726,10 @@ cudaError_t launch_decode_dt(const DecodeParams &p, const CUtensorMap &tk, const
             return e;
         configured = true;
     }
-    // Programmatic stream serialisation: this grid's set-up (barriers, work item)
-    // may overlap the tail of the previous kernel in the stream; the kernel waits
-    // for that kernel's completion before it touches q, the caches or the page table.
+    // Programmatic stream serialisation (overlap_prev): this grid's set-up (barriers,
+    // work item) may overlap the tail of the previous kernel in the stream; the kernel
+    // waits for that kernel's completion before it touches q, the caches or the page
+    // table. Not when the previous kernel writes the work list itself.
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)num_items);
     cfg.blockDim = dim3(Tr::kThreads);
@@ -735,7 +739,7 @@ cudaError_t launch_decode_dt(const DecodeParams &p, const CUtensorMap &tk, const
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = overlap_prev ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, decode_kernel<D, TMA_KV, TT, KV, TPW>, p, tk, tv);
 }
 

@@ -102,6 +102,8 @@ struct DecodeParams {
     float cap_out;
     float v_scale;       // multiplies the final output
     int32_t kv_dtype;    // element type of the caches (pkv_dtype: bf16 or an 8-bit float)
+    int32_t wait_probe;  // nonzero: each CTA's first consuming wait is on a barrier nothing completes
+    long long wait_ns;   // bound of every wait (globaltimer nanoseconds)
 };
 
 struct MergePartialsParams {
@@ -142,7 +144,16 @@ struct PrefillParams {
     int32_t ragged;          // 1: K/V are contiguous [total_kv, H_kv, d], kv_page_begin = token offset
     int32_t total_kv;        // ragged: rows of K/V (bound of their tensor maps)
     int32_t kv_dtype;        // element type of the caches (pkv_dtype: bf16 or an 8-bit float)
+    int32_t wait_probe;      // as in DecodeParams
+    long long wait_ns;       // as in DecodeParams
 };
+
+// Bound of every wait inside the kernels: the descriptor's wait_limit_us, or 2 s.
+constexpr long long kDefaultWaitNs = 2000000000LL;
+inline long long wait_ns_of(const pkv_plan_desc &d)
+{
+    return d.wait_limit_us > 0 ? (long long)d.wait_limit_us * 1000LL : kDefaultWaitNs;
+}
 
 // The logit and output factors of a plan descriptor (k_scale folded into the logit
 // scale; scales <= 0 mean 1; a soft cap <= 0 means none).
@@ -163,8 +174,11 @@ inline LogitFactors logit_factors(const pkv_plan_desc &d)
 }
 
 // Launchers (one per kernel family); return cudaGetLastError() of the launch.
-// tile: KV tokens per stage, 64 or (head_dim <= 128) 32.
-cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile);
+// tile: KV tokens per stage, 64 or (head_dim <= 128) 32. overlap_prev: the kernel's
+// set-up may overlap the previous kernel in the stream (programmatic dependent
+// launch); false when that kernel writes the work list the decode reads first.
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile,
+                          bool overlap_prev = true);
 // KV tile of the decode kernel (head_dim <= 128): 32 tokens (4 CTAs per SM) for
 // short key ranges, which are latency-bound, and for medium ones (<= 1024 keys)
 // whose CTAs need more than one wave at 2 per SM but fit in one at 4; otherwise 64
@@ -195,7 +209,7 @@ bool encode_kv_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_he
                    int num_pages, int box_rows, int kv_dtype);
 // The 8-bit-cache decode kernels (p.kv_dtype = PKV_FP8_E4M3 or PKV_FP8_E5M2).
 cudaError_t launch_decode_kv8(const DecodeParams &p, int head_dim, int num_items, cudaStream_t s, int tile,
-                              bool tma, const CUtensorMap &tk, const CUtensorMap &tv);
+                              bool tma, const CUtensorMap &tk, const CUtensorMap &tv, bool overlap_prev);
 cudaError_t launch_merge_partials(const MergePartialsParams &p, int head_dim, cudaStream_t s);
 cudaError_t launch_merge_state(const void *v_a, const float *s_a, const void *v_b,
                                const float *s_b, void *v_out, float *s_out, int64_t rows,

@@ -58,6 +58,46 @@ int scratch_address(void **out)
     return PKV_OK;
 }
 
+// The work list reaches the device as the by-value arguments of small copy kernels
+// (a kernel's argument block may hold up to 32764 bytes): no host staging buffer
+// has to outlive the call, and nothing makes the host wait for earlier work on the
+// stream, as a copy from pageable host memory would.
+constexpr int kUploadWords = 2040;  // 16-byte words per copy kernel (32640 bytes)
+
+struct UploadBlock {
+    uint4 *dst;
+    int32_t words;
+    int32_t pad;
+    uint4 data[kUploadWords];
+};
+static_assert(sizeof(UploadBlock) <= 32764, "kernel argument block");
+
+__global__ void __launch_bounds__(256) upload_kernel(const __grid_constant__ UploadBlock blk)
+{
+    for (int i = threadIdx.x; i < blk.words; i += blockDim.x)
+        blk.dst[i] = blk.data[i];
+}
+
+// Copy `bytes` (a multiple of 16) from host memory to device address `dst`, one copy
+// kernel per kUploadWords words, enqueued on `stream`.
+cudaError_t upload(uint8_t *dst, const uint8_t *src, size_t bytes, cudaStream_t stream)
+{
+    static thread_local UploadBlock blk;  // argument staging; launches copy it out
+    const size_t words = bytes / 16;
+    for (size_t w0 = 0; w0 < words; w0 += kUploadWords) {
+        const size_t n = std::min<size_t>(kUploadWords, words - w0);
+        blk.dst = reinterpret_cast<uint4 *>(dst) + w0;
+        blk.words = (int32_t)n;
+        blk.pad = 0;
+        std::memcpy(blk.data, src + 16 * w0, 16 * n);
+        upload_kernel<<<1, 256, 0, stream>>>(blk);
+        const cudaError_t ce = cudaGetLastError();
+        if (ce != cudaSuccess)
+            return ce;
+    }
+    return cudaSuccess;
+}
+
 int page_shift(int page_size)
 {
     if (page_size <= 0 || (page_size & (page_size - 1)))
@@ -192,14 +232,15 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
     uint8_t *base = (uint8_t *)base_v;
     cudaStream_t stream = (cudaStream_t)stream_;
 
-    // One host staging image of everything before the partial states, copied in
-    // one transfer (the source is pageable: the copy consumes it before returning).
+    // One host image of everything before the partial states, carried to the device
+    // in the arguments of the copy kernels (their launches copy it out, so the image
+    // may be freed on return).
     std::vector<uint8_t> image(o_pl, 0);
     std::memcpy(image.data() + o_reqs, reqs.data(), sizeof(RequestInfo) * reqs.size());
     std::memcpy(image.data() + o_items, items.data(), sizeof(DecodeItem) * items.size());
     if (!merges.empty())
         std::memcpy(image.data() + o_merge, merges.data(), sizeof(MergeItem) * merges.size());
-    cudaError_t ce = cudaMemcpyAsync(base, image.data(), image.size(), cudaMemcpyHostToDevice, stream);
+    cudaError_t ce = upload(base, image.data(), image.size(), stream);
     if (ce != cudaSuccess)
         return noalloc_fail(PKV_ERR_CUDA, std::string("uploading the work list: ") + cudaGetErrorString(ce));
     // The array keeps the previous call's contents: the status word must restart
@@ -228,14 +269,16 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
     p.cap_in = lf.cap_in;
     p.cap_out = lf.cap_out;
     p.v_scale = lf.v_scale;
+    p.wait_ns = wait_ns_of(*d);  // no status to report a probe's expiry: never probed
     int64_t max_keys = 0;
     for (const DecodeItem &it : items)
         max_keys = std::max<int64_t>(max_keys, it.j1 - it.j0);
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // No overlap with the copy kernels: the decode reads its work item first thing.
     ce = launch_decode(p, d->head_dim, (int)items.size(), stream,
-                       decode_tile_for(d->head_dim, max_keys, (int64_t)items.size(), sms));
+                       decode_tile_for(d->head_dim, max_keys, (int64_t)items.size(), sms), false);
     if (ce != cudaSuccess)
         return noalloc_fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(ce));
     if (!merges.empty()) {

@@ -28,7 +28,8 @@
 // Warps (384 threads): 0-3 softmax + epilogue of Q0, 4-7 of Q1 (thread = TMEM
 // lane = packed row), 8 TMEM allocation, Q loads and MMA issue (one lane), 9 TMA
 // producer of K/V (9-11 gather with cp.async in the other mode).
-// Every wait is bounded (PKV_ERR_TIMEOUT, abort flag, MMA drain, TMEM freed).
+// Every wait is bounded by the plan's wait bound (2 s by default): on expiry
+// PKV_ERR_TIMEOUT, abort flag, copies and MMAs drained, TMEM freed.
 //
 // 8-bit K/V caches (E4M3 / E5M2): warps 9-11 copy the 8-bit rows with cp.async into a
 // two-tile staging area and widen them to f16 into the ring; both MMAs run on f16
@@ -71,7 +72,6 @@ struct PPTraits {
     static_assert(kTmemO + kNQ * D <= kTmemCols && kNQ * kT <= kTmemO, "TMEM budget");
 };
 
-constexpr long long kWaitLimitPP = 4000000000LL;
 // Page-id ring of the cp.async producers, in tiles (ids of kIdRing - 1 tiles in flight).
 constexpr int kIdRing = 3;
 
@@ -99,7 +99,8 @@ struct PPBars {
     static constexpr int kVLand = kOEmpty + 2;   // producer only: a tail V tile has landed
     static constexpr int kDrain = kVLand + 1;
     static constexpr int kQ1 = kDrain + 1;       // 8-bit caches: Q_1 written (128 arrivals; kQ: Q_0)
-    static constexpr int kCount = kQ1 + 1;
+    static constexpr int kNever = kQ1 + 1;       // the wait probe's barrier: nothing completes it
+    static constexpr int kCount = kNever + 1;
 };
 
 template <int D, int MASK, bool TMA_KV, bool RAGGED, int KV = PKV_BF16>
@@ -135,6 +136,14 @@ __global__ void __launch_bounds__(384, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // After an abort, the TMA producers wait (bounded, ignoring the abort flag) for the
+    // K/V tiles whose K went out in the last NS ring positions before n_end, so that no
+    // bulk copy lands in shared memory after the CTA has left.
+    auto drain_tma_tiles = [&](uint32_t n_end) {
+        const uint32_t first = n_end > (uint32_t)NS ? n_end - NS : 0u;
+        for (uint32_t nk = first + (first & 1u); nk < n_end; nk += 2)
+            mbar_wait(bar(B::kFull + nk % NS), (nk / kFullPeriod) & 1, &no_abort, p.wait_ns);
+    };
     // This CTA's work items, in order (the plan balances the lists over the CTAs).
     const int item_lo = p.cta_items[blockIdx.x];
     const int item_hi = p.cta_items[blockIdx.x + 1];
@@ -158,6 +167,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(bar(B::kVLand), 1);
         mbar_init(bar(B::kDrain), 1);
+        mbar_init(bar(B::kNever), 1);
         abort_flag = 0;
         no_abort = 0;
         fence_mbarrier_init();
@@ -271,7 +281,7 @@ __global__ void __launch_bounds__(384, 1)
             float m_used = -INFINITY;
             float l = 0.f;
             for (int j = 0; j < n_tiles; ++j, ++n_s) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull + wg), n_s & 1, abort_v, kWaitLimitPP));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull + wg), n_s & 1, abort_v, p.wait_ns));
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(384, 1)
                     q_unscale = write_q(q_item);
             }
             if (ok && n_tiles > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kOFinal + wg), n_o & 1, abort_v, kWaitLimitPP));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kOFinal + wg), n_o & 1, abort_v, p.wait_ns));
                 tc_fence_after();
             }
             if (!ok)
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(384, 1)
                 }
             };
             auto wait = [&](int b_idx, uint32_t parity) {
-                return mbar_wait(bar(b_idx), parity, abort_v, kWaitLimitPP);
+                return mbar_wait(bar(b_idx), parity, abort_v, p.wait_ns);
             };
             // Q of an item: its tiles by TMA (4-D map over [token, KV head, group, d]).
             auto load_q = [&](int ii) {
@@ -468,6 +478,7 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t n_o[2] = {0, 0};  // items accumulated into O_i: the phase of OEmpty_i
             uint32_t n_q = 0;          // Q loads: the phase of kQ
             uint32_t n_q1 = 0;         // 8-bit caches: Q_1 writes, the phase of kQ1
+            bool probe = p.wait_probe != 0;  // the first K/V wait is on a barrier nothing completes
             bool ok = true;
             int ii = next_busy(item_lo);
             if (!KV8 && ii < item_hi)
@@ -493,8 +504,9 @@ __global__ void __launch_bounds__(384, 1)
                     // 8-bit caches: K and V complete their own slots' barriers (one phase
                     // per use), so S_0 starts as soon as K is widened, V is waited for
                     // before its first P V.
-                    if (!(ok = wait(B::kFull + sK, (nK / (KV8 ? NS : kFullPeriod)) & 1)))
+                    if (!(ok = wait(probe ? B::kNever : B::kFull + sK, (nK / (KV8 ? NS : kFullPeriod)) & 1)))
                         break;
+                    probe = false;
                     if (!TMA_KV)
                         fence_proxy_async_smem();
                     tc_fence_after();
@@ -557,7 +569,7 @@ __global__ void __launch_bounds__(384, 1)
                 abort_flag = 1;
             }
             umma_commit(bar(B::kDrain));
-            mbar_wait(bar(B::kDrain), 0, &no_abort, kWaitLimitPP);
+            mbar_wait(bar(B::kDrain), 0, &no_abort, p.wait_ns);
         }
         __syncwarp();
     } else if (RAGGED) {
@@ -583,7 +595,7 @@ __global__ void __launch_bounds__(384, 1)
                     const uint32_t full = bar(B::kFull + n % NS);  // K and V of the tile complete it
                     for (int isv = 0; isv < 2; ++isv, ++n) {
                         const int s = n % NS;
-                        if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP)) {
+                        if (n >= NS && !mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, p.wait_ns)) {
                             okp = false;
                             break;
                         }
@@ -598,6 +610,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!okp) {
                 record_status(p.status, PKV_ERR_TIMEOUT);
                 abort_flag = 1;
+                drain_tma_tiles(n);
             }
         }
     } else if (TMA_KV) {
@@ -653,7 +666,7 @@ __global__ void __launch_bounds__(384, 1)
                         const int s = n % NS;
                         if (n >= NS) {
                             okp = __all_sync(0xffffffffu, mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v,
-                                                                    kWaitLimitPP));
+                                                                    p.wait_ns));
                             if (!okp)
                                 break;
                         }
@@ -678,7 +691,7 @@ __global__ void __launch_bounds__(384, 1)
                             pg_next = load_id(j + 1);
                         if (vtail) {
                             okp = __all_sync(0xffffffffu,
-                                             mbar_wait(bar(B::kVLand), n_land & 1, abort_v, kWaitLimitPP));
+                                             mbar_wait(bar(B::kVLand), n_land & 1, abort_v, p.wait_ns));
                             ++n_land;
                             if (!okp)
                                 break;
@@ -701,6 +714,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!okp && lane == 0) {
                 record_status(p.status, PKV_ERR_TIMEOUT);
                 abort_flag = 1;
+                drain_tma_tiles(n);
             }
         }
     } else if (!KV8) {
@@ -770,7 +784,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int isv = 0; isv < 2; ++isv, ++n) {
                     const int s = n % NS;
                     const bool w_ok =
-                        n < NS || mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, kWaitLimitPP);
+                        n < NS || mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, p.wait_ns);
                     okp = bar_red_and(1, NP, w_ok);  // every producer takes the same way out
                     if (!okp)
                         break;
@@ -898,7 +912,7 @@ __global__ void __launch_bounds__(384, 1)
                     const uint32_t pos = n + isv;
                     const int s = pos % NS;
                     const bool w_ok =
-                        pos < NS || mbar_wait(bar(B::kEmpty + s), ((pos / NS) - 1) & 1, abort_v, kWaitLimitPP);
+                        pos < NS || mbar_wait(bar(B::kEmpty + s), ((pos / NS) - 1) & 1, abort_v, p.wait_ns);
                     okp = bar_red_and(1, NP, w_ok);  // every producer takes the same way out
                     if (!okp)
                         break;

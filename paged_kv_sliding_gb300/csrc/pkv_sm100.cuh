@@ -45,21 +45,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity)
     return ok != 0;
 }
 
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
 // Wait for the phase with the given parity to complete. Gives up (returns false)
-// when *abort is raised by another thread or after about `limit` clock cycles.
+// when *abort is raised by another thread or after about `limit_ns` nanoseconds.
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, const volatile int *abort,
-                                          long long limit)
+                                          long long limit_ns)
 {
     if (mbar_try_wait(addr, parity))
         return true;
-    const long long t0 = clock64();
+    const unsigned long long t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(addr, parity))
             return true;
         if ((it & 63) == 0) {
             if (*abort)
                 return false;
-            if (clock64() - t0 > limit)
+            if ((long long)(global_ns() - t0) > limit_ns)
                 return false;
         }
     }

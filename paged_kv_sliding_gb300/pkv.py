@@ -76,6 +76,8 @@ class PlanDesc(ctypes.Structure):
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
         ("kv_dtype", ctypes.c_int32),
+        ("wait_limit_us", ctypes.c_int32),
+        ("wait_probe", ctypes.c_int32),
     ]
 
 
@@ -188,13 +190,15 @@ class Plan:
                  sm_scale: Optional[float] = None, qo_indptr=None, q_start=None,
                  fixed_split_size: int = -1, disable_split_kv: bool = False, stream=None,
                  capacity: Optional[dict] = None, logits_soft_cap: float = 0.0, k_scale: float = 1.0,
-                 v_scale: float = 1.0, kv_dtype="bf16"):
+                 v_scale: float = 1.0, kv_dtype="bf16", wait_limit_us: int = 0, wait_probe: bool = False):
         """kind: "prefill", "decode" or "prefill_ragged" (K/V passed to run() are
         contiguous [total_kv, H_kv, d]; kv_indptr counts tokens; no page table).
         capacity={"max_batch": B, "max_total_q": Q}: a capturable plan (its run may
         be captured in a CUDA graph and replayed after update()).
         kv_dtype: element type of the caches, "bf16", "e4m3" or "e5m2" (or the torch
-        dtype); the 8-bit ones are for paged (decode and prefill) plans."""
+        dtype); the 8-bit ones are for paged (decode and prefill) plans.
+        wait_limit_us: bound of every device-side wait (<= 0: 2 s); wait_probe: make
+        each CTA's first consuming wait run out (tests of the timeout path)."""
         self._lib = load_library()
         self._handle = ctypes.c_void_p()
         self.kind = kind
@@ -242,6 +246,8 @@ class Plan:
         d.k_scale = float(k_scale)
         d.v_scale = float(v_scale)
         d.kv_dtype = int(kv_dtype)
+        d.wait_limit_us = int(wait_limit_us)
+        d.wait_probe = 1 if wait_probe else 0
         self._desc = d
         if capacity is None:
             _check(self._lib.pkv_plan_create(ctypes.byref(self._handle), ctypes.byref(d),

@@ -36,7 +36,7 @@ def test_header_declares_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_entry_points():
         assert hasattr(lib, name), name
-    assert lib.pkv_abi_version() == 4
+    assert lib.pkv_abi_version() == 5
 
 
 def test_status_strings(lib):
@@ -184,3 +184,32 @@ def test_ragged_desc_validation_on_the_host(lib):
     assert lib.pkv_plan_create(ctypes.byref(out), ctypes.byref(d), None) == pkv.PKV_ERR_INVALID_ARG
     d.kind = 7
     assert lib.pkv_plan_create(ctypes.byref(out), ctypes.byref(d), None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The binding's ctypes structures have the C header's field offsets and sizes
+    (a C program built against include/pkv.h prints them)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"pkv_plan_desc": pkv.PlanDesc, "pkv_plan_caps": pkv.PlanCaps, "pkv_plan_info": pkv.PlanInfo}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "pkv.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        cname, field, val = line.split()
+        got[(cname, field)] = int(val)
+    for cname, cls in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for fname, _ in cls._fields_:
+            assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
