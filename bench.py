@@ -379,15 +379,105 @@ def run_ours(args, rank, world):
     if clocks:
         line["clocks"] = clocks
 
+    oracle_mod, cores = None, None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle as oracle_mod
+        oracle_mod.build()
+        cores = oracle_mod.set_threads(0)
     if not args.no_extra:
-        line["workloads"] = extra_workloads(pkv, args, peaks, flush)
+        line["workloads"] = extra_workloads(pkv, args, peaks, flush, oracle=oracle_mod, cores=cores)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
+        line["host"] = _host_info()
     return line
 
 
 EXTRA = ("swa_prefill_p1", "swa_prefill_p16", "extend_prefix", "extend_ragged", "long_decode",
          "batch_decode_fp8", "long_decode_fp8", "extend_prefix_fp8")
+
+
+# --------------------------------------------------------------- oracle beside each workload
+
+def _host_info():
+    return {"nproc": os.cpu_count(), "OMP_NUM_THREADS": os.environ.get("OMP_NUM_THREADS")}
+
+
+def _oracle_args(w, **over):
+    a = dict(qo_indptr=w.qo_indptr, kv_indptr=w.kv_indptr, kv_indices=w.kv_indices,
+             kv_last_page_len=w.kv_last_page_len, num_qo_heads=w.num_qo_heads,
+             num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, page_size=w.page_size,
+             window_left=w.window_left, causal=w.causal, sm_scale=w.sm_scale, q=w.q.cpu(),
+             k_cache=w.k_cache.cpu(), v_cache=w.v_cache.cpu(), q_start=w.q_start, num_pages=w.num_pages)
+    a.update(over)
+    return a
+
+
+def extend_sample_rows(w, seed=9):
+    """The seeded row sample of the extend parity tests: every request's first and
+    last 64 rows plus 64 random rows."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b in range(w.batch):
+        lo, hi = int(w.qo_indptr[b]), int(w.qo_indptr[b + 1])
+        sel = set(range(lo, min(hi, lo + 64))) | set(range(max(lo, hi - 64), hi))
+        sel |= set(rng.integers(lo, hi, size=64).tolist())
+        rows.extend(sorted(sel))
+    return np.array(rows)
+
+
+def oracle_prefill(oracle, cores, w, rows=None, note=""):
+    """The oracle on a prefill workload (its device tensors copied to the host), in
+    full or on a row sample; TFLOP/s of algorithmic work, and for a sample the full
+    workload's time extrapolated from that rate."""
+    args = _oracle_args(w)
+    t0 = time.perf_counter()
+    oracle.attention(rows=rows, **args)
+    el = time.perf_counter() - t0
+    full = workcount.attention_flops(w)
+    flops = full if rows is None else workcount.attention_flops_rows(w, rows)
+    r = {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+         "seconds": round(el, 3), "sample": "the full workload" if rows is None else
+         f"{len(rows)} of {int(w.qo_indptr[-1])} query rows (every request's first and last 64 rows "
+         f"and 64 seeded random rows), all heads"}
+    if rows is not None:
+        r["extrapolated_full_s"] = round(full / (flops / el), 3)
+        r["extrapolated"] = True
+    if note:
+        r["note"] = note
+    return r
+
+
+def oracle_decode(oracle, cores, w, n_req=None, seed=44):
+    """The oracle on a decode workload, in full or on n_req seeded requests (their
+    pages gathered on the device and copied to the host); GB/s of visible KV."""
+    import dataclasses
+    if n_req is None or n_req >= w.batch:
+        sub, label = w, "the full workload"
+    else:
+        rng = np.random.default_rng(seed)
+        sel = np.sort(rng.choice(w.batch, size=n_req, replace=False))
+        pages = np.concatenate([w.kv_indices[w.kv_indptr[b]:w.kv_indptr[b + 1]] for b in sel])
+        pidx = torch.as_tensor(pages.astype(np.int64), device=w.k_cache.device)
+        kv_indptr = np.zeros(len(sel) + 1, dtype=np.int32)
+        kv_indptr[1:] = np.cumsum(np.diff(w.kv_indptr)[sel])
+        tsel = torch.as_tensor(sel, device=w.q.device)
+        sub = dataclasses.replace(
+            w, qo_indptr=np.arange(len(sel) + 1, dtype=np.int32), kv_indptr=kv_indptr,
+            kv_indices=np.arange(len(pages), dtype=np.int32), kv_last_page_len=w.kv_last_page_len[sel],
+            num_pages=len(pages), q=w.q[tsel].cpu(), k_cache=w.k_cache[pidx].cpu(),
+            v_cache=w.v_cache[pidx].cpu(), q_start=None if w.q_start is None else w.q_start[sel])
+        label = f"{n_req} of {w.batch} requests (seeded), every head and visible key"
+    args = _oracle_args(sub)
+    t0 = time.perf_counter()
+    oracle.attention(**args)
+    el = time.perf_counter() - t0
+    nbytes = workcount.decode_kv_bytes(sub)
+    r = {"value": round(nbytes / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+         "seconds": round(el, 3), "sample": label}
+    if sub is not w:
+        r["extrapolated_full_s"] = round(workcount.decode_kv_bytes(w) / (nbytes / el), 3)
+        r["extrapolated"] = True
+    return r
 
 
 def bench_prefill_ragged(pkv, w, steps, warmup, flush):
@@ -415,7 +505,10 @@ def bench_prefill_ragged(pkv, w, steps, warmup, flush):
             "work_items": plan.info["num_work_items"]}
 
 
-def extra_workloads(pkv, args, peaks, flush, only=None):
+def extra_workloads(pkv, args, peaks, flush, only=None, oracle=None, cores=None):
+    """The prefill and long-decode workloads on the GPU; with `oracle` given, the
+    float64 oracle is timed on the host beside each one (in full, or on the seeded
+    sample of the parity tests with the full time extrapolated)."""
     res = {}
     steps = max(3, min(args.steps, 10))
     want = lambda n: only is None or only == n  # noqa: E731
@@ -425,27 +518,37 @@ def extra_workloads(pkv, args, peaks, flush, only=None):
         w = wl.swa_prefill(page_size=P, device="cuda")
         r = bench_prefill(pkv, w, steps, 3, flush)
         r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
+        if oracle is not None:
+            r["cpu_baseline"] = oracle_prefill(oracle, cores, w)
         res[f"swa_prefill_8x1500_d256_W511_p{P}"] = r
         del w
-    if want("extend_prefix"):
+    if want("extend_prefix") or want("extend_ragged"):
         w = wl.extend_with_prefix(device="cuda")
-        r = bench_prefill(pkv, w, steps, 3, flush)
-        r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
-        res["extend_prefix_16req_W4095"] = r
+        ext_cpu = oracle_prefill(oracle, cores, w, rows=extend_sample_rows(w)) if oracle is not None else None
+        if want("extend_prefix"):
+            r = bench_prefill(pkv, w, steps, 3, flush)
+            r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
+            r["traffic"] = _profiled_traffic("prefill", "extend_with_prefix", "pkv_prefill_kernel.cuh")
+            if ext_cpu is not None:
+                r["cpu_baseline"] = ext_cpu
+            res["extend_prefix_16req_W4095"] = r
+        if want("extend_ragged"):
+            r = bench_prefill_ragged(pkv, w, steps, 3, flush)
+            r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
+            if ext_cpu is not None:
+                r["cpu_baseline"] = dict(ext_cpu, note="the same oracle computation as the paged extend "
+                                                       "(the oracle walks a page table; the ragged path "
+                                                       "computes the same attention)")
+            res["extend_prefix_16req_W4095_ragged_kv"] = r
         del w
         torch.cuda.empty_cache()
     if want("extend_prefix_fp8"):
         w = wl.to_kv8(wl.extend_with_prefix(device="cuda"), "e4m3")
         r = bench_prefill(pkv, w, steps, 3, flush)
         r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]  # f16 MMAs run at the bf16 rate
+        if oracle is not None:
+            r["cpu_baseline"] = oracle_prefill(oracle, cores, w, rows=extend_sample_rows(w))
         res["extend_prefix_16req_W4095_e4m3"] = r
-        del w
-        torch.cuda.empty_cache()
-    if want("extend_ragged"):
-        w = wl.extend_with_prefix(device="cuda")
-        r = bench_prefill_ragged(pkv, w, steps, 3, flush)
-        r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
-        res["extend_prefix_16req_W4095_ragged_kv"] = r
         del w
         torch.cuda.empty_cache()
     for W in (wl.LONG_DECODE_WINDOWS if want("long_decode") else ()):
@@ -456,8 +559,12 @@ def extra_workloads(pkv, args, peaks, flush, only=None):
             "gbs": bytes_per[0] / (k * 1e-3) / 1e9, "kernel_ms": k,
             "step_ms": statistics.mean(step_ms), "kv_gb": bytes_per[0] / 1e9,
             "frac_hbm": bytes_per[0] / (k * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "frac_note": "the peak is a copy's (read + write) rate; this kernel only reads",
             "splits": plans[0].info["num_partials"], "ctas": plans[0].info["num_work_items"]}
-        del w, plans, runs
+        del plans, runs
+        if oracle is not None:
+            res[f"long_decode_256x32768_W{W}"]["cpu_baseline"] = oracle_decode(oracle, cores, w, n_req=32)
+        del w
         torch.cuda.empty_cache()
     # 8-bit KV caches (E4M3): the batch-decode windows and the long decode. GB/s counts
     # the bytes of the 8-bit cache a pass must read (half of bf16's per key).
@@ -472,6 +579,8 @@ def extra_workloads(pkv, args, peaks, flush, only=None):
                 "frac_hbm": bytes_per[i] / (k * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "keys_per_s": bytes_per[i] / (2 * w.num_kv_heads * w.head_dim) / (k * 1e-3),
                 "kv_tile": plans[i].info["kv_tile"], "ctas": plans[i].info["num_work_items"]}
+            if oracle is not None:
+                res[f"batch_decode_e4m3_W{W}"]["cpu_baseline"] = oracle_decode(oracle, cores, w.with_window(W))
         res["batch_decode_e4m3_step_ms"] = statistics.mean(step_ms)
         del w, plans, runs
         torch.cuda.empty_cache()
@@ -485,8 +594,12 @@ def extra_workloads(pkv, args, peaks, flush, only=None):
         res["long_decode_256x32768_W-1_e4m3"] = {
             "gbs": bytes_per[0] / (k * 1e-3) / 1e9, "kernel_ms": k, "kv_gb": bytes_per[0] / 1e9,
             "frac_hbm": bytes_per[0] / (k * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "frac_note": "the peak is a copy's (read + write) rate; this kernel only reads",
             "splits": plans[0].info["num_partials"], "ctas": plans[0].info["num_work_items"]}
-        del w, plans, runs
+        del plans, runs
+        if oracle is not None:
+            res["long_decode_256x32768_W-1_e4m3"]["cpu_baseline"] = oracle_decode(oracle, cores, w, n_req=32)
+        del w
         torch.cuda.empty_cache()
     return res
 
@@ -520,7 +633,7 @@ def cpu_baseline(args, budget_s: float = 12.0):
             break
     return {"value": round(reps * step_bytes / el / 1e9, 4), "unit": UNIT, "cores": cores,
             "kind": "oracle", "sample": f"{reps} full batch-decode step(s) (64 requests x 5 windows), "
-                                        f"{el:.1f} s wall", "seconds": round(el, 2)}
+                                        f"{el:.1f} s wall", "seconds": round(el, 2), **_host_info()}
 
 
 def run_reference(args, rank, world):

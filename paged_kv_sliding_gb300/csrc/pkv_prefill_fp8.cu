@@ -12,9 +12,9 @@ cudaError_t launch_kv(const PrefillParams &p, int head_dim, int mask_mode, int n
 {
     const CUtensorMap none{};
     switch (head_dim) {
-    case 64: return pp::launch_pp_dt<64, false, false, KV>(p, mask_mode, none, none, none, num_ctas, s);
-    case 128: return pp::launch_pp_dt<128, false, false, KV>(p, mask_mode, none, none, none, num_ctas, s);
-    case 256: return pp::launch_pp_dt<256, false, false, KV>(p, mask_mode, none, none, none, num_ctas, s);
+    case 64: return pp::launch_pp_dt<64, false, false, KV>(p, mask_mode, none, none, none, none, num_ctas, s);
+    case 128: return pp::launch_pp_dt<128, false, false, KV>(p, mask_mode, none, none, none, none, num_ctas, s);
+    case 256: return pp::launch_pp_dt<256, false, false, KV>(p, mask_mode, none, none, none, none, num_ctas, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -40,3 +40,16 @@ def decode_kv_bytes(w: Workload) -> int:
     """Bytes of K and V a decode pass must read: visible rows x 2 x H_kv x d x the
     cache's element size (2 B for bf16, 1 B for an 8-bit cache)."""
     return visible_pairs_per_head(w) * 2 * w.num_kv_heads * w.head_dim * w.k_cache.element_size()
+
+
+def attention_flops_rows(w: Workload, rows) -> int:
+    """Algorithmic flops of a subset of query rows (global row indices): 4 * d * H_qo
+    per visible (row, key) pair, by the same interval arithmetic."""
+    rows = np.asarray(rows, dtype=np.int64)
+    req = np.searchsorted(w.qo_indptr, rows, side="right") - 1
+    L = w.kv_lens[req].astype(np.int64)
+    start = (w.q_start[req].astype(np.int64) if w.q_start is not None else L - w.qo_lens[req])
+    p = start + (rows - w.qo_indptr[req])
+    hi = np.minimum(p, L - 1) if w.causal else L - 1
+    lo = np.maximum(p - w.window_left, 0) if w.window_left >= 0 else np.zeros_like(p)
+    return 4 * w.head_dim * w.num_qo_heads * int(np.clip(hi - lo + 1, 0, None).sum())

@@ -52,3 +52,23 @@ def test_decode_kv_bytes(W):
     rows = sum(min(L, W + 1) if W >= 0 else L for L in (1, 100, 300))
     assert workcount.decode_kv_bytes(w) == rows * 2 * 2 * 64 * 2
     assert workcount.decode_kv_bytes(wl.to_kv8(w, "e4m3")) == rows * 2 * 2 * 64 * 1
+
+
+@pytest.mark.parametrize("W", [-1, 0, 3, 17])
+@pytest.mark.parametrize("causal", [True, False])
+def test_row_subset_flops_match_brute_force(W, causal):
+    """The flops of a row subset (the bench's sampled oracle timing) equal 4 d H_qo
+    times the brute-force visible pairs of exactly those rows; all rows give the total."""
+    w = wl.make_workload(name="wc", qo_lens=[5, 0, 9, 1], kv_lens=[12, 4, 9, 30], num_qo_heads=2,
+                         num_kv_heads=1, head_dim=64, page_size=4, window_left=W, causal=causal, seed=3,
+                         q_start=[2, 0, -3, 40])
+    rows = np.array([0, 4, 5, 7, 13, 14])
+    n = 0
+    for r in rows:
+        b = int(np.searchsorted(w.qo_indptr, r, side="right") - 1)
+        p = int(w.q_start[b]) + int(r - w.qo_indptr[b])
+        for j in range(int(w.kv_lens[b])):
+            if (not causal or j <= p) and (W < 0 or j >= p - W):
+                n += 1
+    assert workcount.attention_flops_rows(w, rows) == 4 * 64 * 2 * n
+    assert workcount.attention_flops_rows(w, np.arange(15)) == workcount.attention_flops(w)
