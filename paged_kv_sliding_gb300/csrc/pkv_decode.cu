@@ -18,9 +18,24 @@ bool encode_kv_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_he
             return false;
         fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
     }
-    // Boxes of one 128-byte plane (64 bf16 or 128 8-bit elements) x rows of one page;
-    // an 8-bit row of d 64 is a single 64-byte plane with the 64-byte swizzle.
     const int eb = kv_dtype == PKV_BF16 ? 2 : 1;
+    if (eb == 2) {
+        // bf16: the pool as 5-D [8-row blocks][H_kv][128-byte plane][row in block][64]
+        // (a page of a multiple of 8 rows is a run of 8-row blocks); a box of box_rows
+        // rows of one KV head and every plane lands as box_rows / 8 group-major row
+        // groups of the kernel's stage.
+        const cuuint64_t row = (cuuint64_t)num_kv_heads * head_dim * 2;
+        const cuuint64_t blocks = (cuuint64_t)(num_pages > 0 ? num_pages : 1) * (cuuint64_t)page_size / 8;
+        const cuuint64_t dims5[5] = {64, 8, (cuuint64_t)head_dim / 64, (cuuint64_t)num_kv_heads, blocks};
+        const cuuint64_t strides5[4] = {row, 128, (cuuint64_t)head_dim * 2, 8 * row};
+        const cuuint32_t box5[5] = {64, 8, (cuuint32_t)head_dim / 64, 1, (cuuint32_t)box_rows / 8};
+        const cuuint32_t estr5[5] = {1, 1, 1, 1, 1};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims5, strides5, box5, estr5,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    // 8-bit: boxes of one 128-byte plane (128 elements) x rows of one page; an 8-bit row
+    // of d 64 is a single 64-byte plane with the 64-byte swizzle.
     const int row_bytes = head_dim * eb;
     const int plane = row_bytes < 128 ? row_bytes : 128;
     const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)page_size,

@@ -73,11 +73,17 @@ struct DecTraits {
 // planes of PR-byte rows: PR = 128 with the 128-byte XOR swizzle (the layout a
 // SWIZZLE_128B TMA box produces; granules 8 apart sit in the next plane), or PR = 64
 // (one 64-byte row per token, 8-bit d 64) with the 64-byte swizzle of SWIZZLE_64B.
-template <int TT, int PR = 128>
+// GM > 0 (bf16 caches, GM = 128-byte planes per row): group-major, 8-row groups of all
+// GM planes [TT/8][GM][8 rows][128 B], so that one TMA box of a page brings every
+// plane of its rows; otherwise plane-major [planes][TT rows][PR bytes].
+template <int TT, int PR = 128, int GM = 0>
 __device__ __forceinline__ uint32_t plane_off(int row, int c16)
 {
     if (PR == 64)
         return (uint32_t)(row * 64 + (((c16 & 3) ^ ((row >> 1) & 3)) << 4));
+    if (GM > 0)
+        return (uint32_t)((row >> 3) * (GM * 1024) + (c16 >> 3) * 1024 + (row & 7) * 128 +
+                          (((c16 & 7) ^ (row & 7)) << 4));
     return (uint32_t)((c16 >> 3) * (TT * 128) + row * 128 + (((c16 & 7) ^ (row & 7)) << 4));
 }
 
@@ -121,6 +127,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
     constexpr int NSB = TPW / 16;  // 16-token sub-blocks per compute warp
     constexpr bool KV8 = KV != PKV_BF16;
     constexpr int PR = Tr::kPlaneRow;
+    constexpr int GM = KV8 ? 0 : Tr::kNCh;  // bf16: group-major stages (one TMA box per page)
     constexpr int S = Tr::kStages;
     constexpr int NW = Tr::kCompute;
     constexpr int NT = 32 * NW;  // compute threads
@@ -215,11 +222,19 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
                 if (pg >= 0) {
                     const uint32_t kb = ring + s * Tr::kStageBytes;
                     const uint32_t vb = kb + Tr::kTileBytes;
-                    for (int c = 0; c < Tr::kNCh; ++c) {
-                        const uint32_t o = c * Tr::kPlaneBytes + lane * rows_box * PR;
-                        const int x = c * (PR / Tr::kElem);  // first element of the plane
-                        tma_load_4d(kb + o, &tm_k, x, it.kv_head, slot0, pg, smem_u32(&full_bar[s]));
-                        tma_load_4d(vb + o, &tm_v, x, it.kv_head, slot0, pg, smem_u32(&full_bar[s]));
+                    if (GM > 0) {
+                        // one 5-D box [8-row blocks][H_kv][plane][8 rows][64] per page: all planes
+                        const uint32_t o = (uint32_t)(lane * rows_box / 8) * (GM * 1024);
+                        const int blk = (pg * P + slot0) >> 3;
+                        tma_load_5d(kb + o, &tm_k, 0, 0, 0, it.kv_head, blk, smem_u32(&full_bar[s]));
+                        tma_load_5d(vb + o, &tm_v, 0, 0, 0, it.kv_head, blk, smem_u32(&full_bar[s]));
+                    } else {
+                        for (int c = 0; c < Tr::kNCh; ++c) {
+                            const uint32_t o = c * Tr::kPlaneBytes + lane * rows_box * PR;
+                            const int x = c * (PR / Tr::kElem);  // first element of the plane
+                            tma_load_4d(kb + o, &tm_k, x, it.kv_head, slot0, pg, smem_u32(&full_bar[s]));
+                            tma_load_4d(vb + o, &tm_v, x, it.kv_head, slot0, pg, smem_u32(&full_bar[s]));
+                        }
                     }
                 }
                 issued = t + 1;
@@ -259,8 +274,8 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
                     }
 #pragma unroll
                     for (int c = 0; c < CH; ++c) {
-                        cp_async_16(kb + plane_off<TT, PR>(row, c), kcache + off + c * 16, bytes);
-                        cp_async_16(vb + plane_off<TT, PR>(row, c), vcache + off + c * 16, bytes);
+                        cp_async_16(kb + plane_off<TT, PR, GM>(row, c), kcache + off + c * 16, bytes);
+                        cp_async_16(vb + plane_off<TT, PR, GM>(row, c), vcache + off + c * 16, bytes);
                     }
                 }
                 cp_async_mbar_arrive(smem_u32(&full_bar[s]));
@@ -368,7 +383,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
                     const int row = warp * TPW + e / Tr::kGran, c = e % Tr::kGran;
                     const int j = tb + t * TT + row;
                     if (j < it.j0 || j >= it.j1)
-                        *reinterpret_cast<uint4 *>(vgen + plane_off<TT, PR>(row, c)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vgen + plane_off<TT, PR, GM>(row, c)) = make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
             }
@@ -394,7 +409,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
                         const int row = row0 + ((mi >> 1) << 3) + (lane & 7);
                         const int c16 = 2 * ks + (mi & 1);
                         uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(kb + plane_off<TT>(row, c16), b0, b1, b2, b3);
+                        ldmatrix_x4(kb + plane_off<TT, 128, GM>(row, c16), b0, b1, b2, b3);
                         float (&acc)[2][4] = (ks & 1) ? sc2[b] : sc[b];
                         mma_bf16_16816(acc[0], qf[ks], b0, b1);
                         mma_bf16_16816(acc[1], qf[ks], b2, b3);
@@ -408,7 +423,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
                         const int mi = lane >> 3;
                         const int row = row0 + ((mi & 1) << 3) + (lane & 7);
                         uint32_t w[4];
-                        ldmatrix_x4(kb + plane_off<TT, PR>(row, 2 * kk + (mi >> 1)), w[0], w[1], w[2], w[3]);
+                        ldmatrix_x4(kb + plane_off<TT, PR, GM>(row, 2 * kk + (mi >> 1)), w[0], w[1], w[2], w[3]);
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             uint32_t b0, b1;
@@ -506,7 +521,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
                         const int row = row0 + ((mi & 1) << 3) + (lane & 7);
                         const int c16 = 2 * np + (mi >> 1);
                         uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(vb + plane_off<TT>(row, c16), b0, b1, b2, b3);
+                        ldmatrix_x4_trans(vb + plane_off<TT, 128, GM>(row, c16), b0, b1, b2, b3);
                         mma_bf16_16816(o[2 * np], pa, b0, b1);
                         mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
                     }
@@ -523,7 +538,7 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
                         const int mi = lane >> 3;
                         const int row = row0 + ((mi & 1) << 3) + (lane & 7);
                         uint32_t w[4];
-                        ldmatrix_x4_trans(vb + plane_off<TT, PR>(row, 2 * kk + (mi >> 1)), w[0], w[1], w[2], w[3]);
+                        ldmatrix_x4_trans(vb + plane_off<TT, PR, GM>(row, 2 * kk + (mi >> 1)), w[0], w[1], w[2], w[3]);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {  // granule 2kk + h: words 2h (tokens 0-7), 2h+1 (8-15)
                             uint32_t e0, o0, e1, o1;

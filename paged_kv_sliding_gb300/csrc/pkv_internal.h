@@ -203,8 +203,10 @@ inline int decode_kernel_tile(int tile, int head_dim, int kv_dtype)
 }
 // Page sizes whose pages the decode kernel loads with TMA boxes of a `tile`-token stage.
 bool decode_tma_page_size(int page_size, int tile);
-// 4-D tensor map [page, slot, KV head, d] over a cache of kv_dtype elements, boxes of
-// one 128-byte plane (64 bytes for 8-bit d 64) x box_rows slots.
+// Tensor map over a cache of kv_dtype elements for the decode kernel's TMA page boxes:
+// bf16, 5-D [8-row blocks][KV head][128-byte plane][row in block][64], one box = box_rows
+// rows of one KV head with every plane (the group-major stage layout); 8-bit, 4-D
+// [page, slot, KV head, d], one box = one 128-byte plane (64 bytes at d 64) x box_rows.
 bool encode_kv_map(CUtensorMap *m, const void *base, int head_dim, int num_kv_heads, int page_size,
                    int num_pages, int box_rows, int kv_dtype);
 // The 8-bit-cache decode kernels (p.kv_dtype = PKV_FP8_E4M3 or PKV_FP8_E5M2).
