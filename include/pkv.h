@@ -39,6 +39,10 @@
  * [0, num_pages) in kv_indices) are recorded by the kernels in a device status
  * word instead of being dereferenced; read it with pkv_plan_device_status().
  *
+ * Tracing: the host side of every entry point is an NVTX range named after it
+ * ("pkv_run decode" / "pkv_run prefill" for runs), shown by profilers' timelines; with
+ * no tool attached the range calls return at once.
+ *
  * Threading and streams: a plan may be run from one host thread at a time; all
  * launches are asynchronous on the caller's stream (a cudaStream_t passed as void*,
  * NULL = legacy default stream). pkv_run and pkv_merge_state never synchronise;

@@ -18,6 +18,7 @@
 #include <vector>
 
 #include "pkv_internal.h"
+#include "pkv_nvtx.h"
 
 using namespace pkv;
 
@@ -665,12 +666,14 @@ int create_plan(pkv_plan **out, const pkv_plan_desc *desc, const pkv_plan_caps *
 
 int pkv_plan_create(pkv_plan **out, const pkv_plan_desc *desc, void *stream)
 {
+    NvtxRange range("pkv_plan_create");
     return create_plan(out, desc, nullptr, stream);
 }
 
 int pkv_plan_create_capturable(pkv_plan **out, const pkv_plan_desc *desc, const pkv_plan_caps *caps,
                                void *stream)
 {
+    NvtxRange range("pkv_plan_create_capturable");
     if (!caps) {
         g_last_error.clear();
         if (out)
@@ -682,6 +685,7 @@ int pkv_plan_create_capturable(pkv_plan **out, const pkv_plan_desc *desc, const 
 
 int pkv_plan_update(pkv_plan *plan, const pkv_plan_desc *desc, void *stream_)
 {
+    NvtxRange range("pkv_plan_update");
     g_last_error.clear();
     if (!plan)
         return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
@@ -822,6 +826,7 @@ static bool misaligned(const void *p, uintptr_t a) { return ((uintptr_t)p) % a !
 int pkv_run(const pkv_plan *plan, const void *q, const void *k_cache, const void *v_cache, void *out,
             float *lse, void *stream_)
 {
+    NvtxRange range(plan && plan->desc.kind == PKV_DECODE ? "pkv_run decode" : "pkv_run prefill");
     g_last_error.clear();
     if (!plan)
         return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
@@ -931,6 +936,7 @@ int pkv_merge_state(const void *v_a, const float *s_a, const void *v_b, const fl
                     float *s_out, int64_t n_tokens, int32_t n_heads, int32_t head_dim, int32_t dtype,
                     void *stream)
 {
+    NvtxRange range("pkv_merge_state");
     g_last_error.clear();
     if (n_tokens < 0 || n_heads < 0)
         return fail(PKV_ERR_INVALID_ARG, "negative size");

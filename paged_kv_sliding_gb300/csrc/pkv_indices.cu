@@ -12,6 +12,7 @@
 // Every read and write is bounds-checked; a violation is recorded in the optional
 // status word (PKV_ERR_DEVICE_BOUNDS) and the offending entries are skipped.
 #include "pkv_internal.h"
+#include "pkv_nvtx.h"
 #include "pkv_ptx.cuh"
 
 namespace pkv {
@@ -122,6 +123,7 @@ extern "C" PKV_API int pkv_build_kv_indices(const int32_t *req_to_token, int32_t
                                             int64_t kv_indices_capacity, int32_t *status, void *stream_)
 {
     using namespace pkv;
+    NvtxRange range("pkv_build_kv_indices");
     if (batch_size < 0 || num_rows < 0 || row_stride < 0 || kv_indices_capacity < 0 || loc_map_len < 0) {
         set_last_error("pkv_build_kv_indices: negative size");
         return PKV_ERR_INVALID_ARG;

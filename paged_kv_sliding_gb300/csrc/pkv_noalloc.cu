@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "pkv_internal.h"
+#include "pkv_nvtx.h"
 
 namespace {
 
@@ -114,6 +115,7 @@ extern "C" int pkv_decode_noalloc(const pkv_plan_desc *d, const void *q, const v
                                   const void *v_cache, void *out, float *lse, void *stream_)
 {
     using namespace pkv;
+    NvtxRange range("pkv_decode_noalloc");
     pkv::set_last_error("");
     if (!d || d->kind != PKV_DECODE)
         return noalloc_fail(PKV_ERR_INVALID_ARG, "needs a PKV_DECODE description");
