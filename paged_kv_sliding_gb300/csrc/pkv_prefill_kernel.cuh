@@ -141,6 +141,13 @@ __global__ void __launch_bounds__(384, 1)
     // One query tile per item (head_dim 256, bf16 caches): S is double-buffered in TMEM
     // (S(j+1) is computed while the softmax works on S(j)); the softmax warpgroup is 0.
     constexpr bool kDS = Tr::kNQ == 1 && !KV8;
+    // With TMA page boxes, warpgroup 1 writes Q into TMEM (the S MMAs' A operand) and
+    // full items' outputs leave through the Q tile's shared memory. With cp.async
+    // gathers, warpgroup 1 gathers K/V beside warps 9-11 instead (224 producers: the
+    // row gather, not the tensor core, bounds that case), Q stays in shared memory.
+    constexpr bool kQTM = kDS && TMA_KV;
+    constexpr bool kWideGather = kDS && !TMA_KV;
+    constexpr int kGP = kWideGather ? 224 : Tr::kProducers;  // cp.async gather threads
     // Ring slot layout. Paged bf16 caches: group-major, [T/8 key groups][NCH column
     // chunks][8 keys][128 B] (one 1 KB swizzle atom per group and chunk), so that one TMA
     // box of a page carries every column chunk of its rows. Otherwise chunk-major,
@@ -189,10 +196,10 @@ __global__ void __launch_bounds__(384, 1)
     const volatile int *abort_v = &abort_flag;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(B::kQ), (KV8 || Tr::kQTmem) ? 128 : 1);
+        mbar_init(bar(B::kQ), (KV8 || kQTM) ? 128 : 1);
         mbar_init(bar(B::kQ1), 128);
         for (int s = 0; s < NS; ++s) {
-            mbar_init(bar(B::kFull + s), TMA_KV ? 1 : Tr::kProducers);
+            mbar_init(bar(B::kFull + s), TMA_KV ? 1 : kGP);
             mbar_init(bar(B::kEmpty + s), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -231,8 +238,119 @@ __global__ void __launch_bounds__(384, 1)
     else
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsSoftmax));
 
+    // cp.async producers of bf16 K/V (page sizes TMA boxes do not suit): thread pt of NP
+    // (warps 9-11, and with one query tile warpgroup 1 too).
+    auto gather = [&](const int pt) {
+            // Work unit = one row and kGU consecutive 16-byte granules of one 64-column
+            // chunk's 128-byte line (8, or 4 with 224 producers): one page-table lookup feeds
+            // kGU copies (fewer instructions per byte than a granule per lane, which measured
+            // slower here although its warp instructions read whole lines). Rows past the
+            // cache end are zero-filled. The page id of every row is fetched kIdRing - 1
+            // tiles ahead into the shared ring by cp.async (the producers never stall on a
+            // page-table read); named barrier 1 orders the ring among the producers.
+            constexpr int NP = kGP;
+            constexpr int kGU = kWideGather ? 4 : 8;
+            constexpr int kUPR = CH / kGU;  // units per row
+            constexpr int kUnits = T * kUPR;
+            int c_ii = item_lo, c_j = 0, c_at = -1;
+            PrefillItem c_it{};
+            int c_kv_len = 0, c_page_begin = 0;
+            uint32_t n_ids = 0;
+            auto fetch_ids = [&]() {
+                while (c_ii < item_hi) {
+                    if (c_at != c_ii) {
+                        c_it = p.items[c_ii];
+                        const RequestInfo r = p.reqs[c_it.req];
+                        c_kv_len = r.kv_len;
+                        c_page_begin = r.kv_page_begin;
+                        c_at = c_ii;
+                    }
+                    if (c_j < c_it.kv_tiles)
+                        break;
+                    ++c_ii;
+                    c_j = 0;
+                }
+                if (c_ii < item_hi) {
+                    const int j0 = prefill_kv_key_at(c_it, c_j, T);
+                    for (int t = pt; t < T; t += NP) {
+                        int *dst = &id_ring[(n_ids % kIdRing) * Tr::kIdsPerTile + t];
+                        const int jj = j0 + t;
+                        if (jj < c_kv_len) {
+                            const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
+                            cp_async_4(smem_u32(dst), p.kv_indices + c_page_begin + lp);
+                        } else {
+                            *dst = -1;
+                        }
+                    }
+                }
+                cp_async_commit();
+                ++c_j;
+                ++n_ids;
+            };
+            auto sync_producers = [] { asm volatile("bar.sync 1, %0;\n" ::"n"(NP) : "memory"); };
+            for (int k = 0; k < kIdRing - 1; ++k)
+                fetch_ids();
+            uint32_t n = 0;    // K/V ring position
+            uint32_t n_t = 0;  // tiles gathered so far
+            bool okp = true;
+            for (int ii = item_lo; okp && ii < item_hi; ++ii) {
+                const PrefillItem it = p.items[ii];
+                const int n_tiles = it.kv_tiles;
+                if (n_tiles <= 0)
+                    continue;
+                for (int j = 0; okp && j < n_tiles; ++j, ++n_t) {
+                    const int j0 = prefill_kv_key_at(it, j, T);
+                    sync_producers();  // every producer is done with the ring entry refilled next
+                    fetch_ids();
+                    cp_async_wait<kIdRing - 1>();
+                    sync_producers();  // this tile's ids are visible to all producers
+                    const int *ids = &id_ring[(n_t % kIdRing) * Tr::kIdsPerTile];
+                    const uint32_t full = bar(B::kFull + n % NS);  // K and V of the tile complete it
+                    for (int isv = 0; isv < 2; ++isv, ++n) {
+                        const int s = n % NS;
+                        const bool w_ok =
+                            n < NS || mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, p.wait_ns);
+                        okp = bar_red_and(1, NP, w_ok);  // every producer takes the same way out
+                        if (!okp)
+                            break;
+                        const uint16_t *src = isv ? p.v_cache : p.k_cache;
+                        for (int u = pt; u < kUnits; u += NP) {
+                            const int t = u / kUPR, q0 = (u % kUPR) * kGU;  // row, first granule
+                            const int jj = j0 + t;
+                            const int page = ids[t];
+                            size_t off = 0;
+                            uint32_t bytes = 0;
+                            if (page >= 0) {
+                                if ((unsigned)page < (unsigned)p.num_pages) {
+                                    const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
+                                    const int sl = jj - lp * p.page_size;
+                                    off = (((size_t)page * p.page_size + sl) * p.num_kv_heads + it.kv_head) * D + q0 * 8;
+                                    bytes = 16;
+                                } else if (isv == 0) {
+                                    record_status(p.status, PKV_ERR_DEVICE_BOUNDS);
+                                }
+                            }
+                            const uint32_t line = slot(s) + slot_line(t, q0 >> 3);
+    #pragma unroll
+                            for (int c = 0; c < kGU; ++c)
+                                cp_async_16(line + ((((q0 & 7) + c) ^ (t & 7)) << 4), src + off + c * 8, bytes);
+                        }
+                        if (isv == 1)
+                            cp_async_mbar_arrive(full);
+                    }
+                }
+            }
+            if (!okp) {
+                record_status(p.status, PKV_ERR_TIMEOUT);
+                abort_flag = 1;
+            }
+            asm volatile("cp.async.wait_all;\n" ::: "memory");
+    };
+
     if (warp < 8) {
-        if (kDS && warp >= 4) {
+        if (kWideGather && warp >= 4) {
+            gather(96 + (threadIdx.x - 128));
+        } else if (kQTM && warp >= 4) {
             // ------------------------------------------------------------ Q into TMEM
             // Warpgroup 1 (idle as a softmax group with one query tile) writes each
             // item's Q tile into TMEM, thread = lane = packed row (token r / g, head
@@ -521,7 +639,7 @@ __global__ void __launch_bounds__(384, 1)
                 // shared memory, in the layout of the output tensor map's boxes, and
                 // leave as one TMA store per 64-column chunk (whole lines, where a
                 // thread-per-row store would touch 32 lines per instruction).
-                const bool staged = kDS && n_tiles > 0 && ntok_wg == tq;
+                const bool staged = kQTM && n_tiles > 0 && ntok_wg == tq;
                 if (staged) {
                     if (r == 0) {
                         bulk_wait_read0();  // the previous item's stores have read the tile
@@ -594,7 +712,7 @@ __global__ void __launch_bounds__(384, 1)
                 record_status(p.status, PKV_ERR_TIMEOUT);
                 abort_flag = 1;
             }
-            if (kDS && threadIdx.x == 0)
+            if (kQTM && threadIdx.x == 0)
                 bulk_wait0();  // the output stores are done before the CTA leaves
         }
     } else if (warp == 8) {
@@ -654,7 +772,7 @@ __global__ void __launch_bounds__(384, 1)
             bool probe = p.wait_probe != 0;  // the first K/V wait is on a barrier nothing completes
             bool ok = true;
             int ii = next_busy(item_lo);
-            if (!KV8 && !kDS && ii < item_hi)
+            if (!KV8 && !kQTM && ii < item_hi)
                 load_q(ii);
             // One query tile, S double-buffered: per item, S(0), then for each KV tile j
             // S(j+1) (into the other buffer) before O += P(j) V(j), so that the tensor
@@ -688,19 +806,28 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint64_t b = sdesc_sw128(kslot + (k >> 2) * kChunkStride + (k & 3) * 32, 16, kGroupStride);
-                        umma_f16_ts(dst, tmem + Tr::kTmemQ + k * 8, b, idesc_s, k > 0 ? 1u : 0u);
+                        if (kQTM) {
+                            umma_f16_ts(dst, tmem + Tr::kTmemQ + k * 8, b, idesc_s, k > 0 ? 1u : 0u);
+                        } else {
+                            const uint64_t a = sdesc_sw128(sQ + (k >> 2) * (128 * Tr::kChunk) + (k & 3) * 32, 16, 1024);
+                            umma_f16(dst, a, b, idesc_s, k > 0 ? 1u : 0u);
+                        }
                     }
                     umma_commit(bar(B::kSFull + (n_sq & 1)));
                     umma_commit(bar(B::kEmpty + sK));
                     ++n_sq;
                     return true;
                 };
-                // the item's last S has completed: Q (in TMEM) is free for the next item
+                // the item's last S has completed: Q (in TMEM, or its shared tile) is free
+                // for the next item
                 auto next_q = [&]() -> bool {
                     const uint32_t m = n_sq - 1;
                     if (!wait(B::kSFull + (m & 1), (m >> 1) & 1))
                         return false;
-                    mbar_arrive(bar(B::kQFree));
+                    if (kQTM)
+                        mbar_arrive(bar(B::kQFree));
+                    else
+                        load_q(ii_next);
                     return true;
                 };
                 uint32_t sv_cur = 0, sv_next = 0;
@@ -983,109 +1110,7 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (!KV8) {
         // ------------------------------------------------------------ cp.async producers
-        constexpr int NP = Tr::kProducers;
-        const int pt = threadIdx.x - 9 * 32;
-        // Work unit = one row and 8 consecutive 16-byte chunks (one 128-byte line of a
-        // 64-column chunk): one page-table lookup feeds 8 copies (fewer instructions per
-        // byte than a granule per lane, which measured slower here although its warp
-        // instructions read whole lines). Rows past the cache end are zero-filled. The
-        // page id of every row is fetched kIdRing - 1 tiles ahead into the shared ring
-        // by cp.async (the producers never stall on a page-table read); named barrier 1
-        // orders the ring among the producers.
-        constexpr int kUnits = T * (CH / 8);
-        int c_ii = item_lo, c_j = 0, c_at = -1;
-        PrefillItem c_it{};
-        int c_kv_len = 0, c_page_begin = 0;
-        uint32_t n_ids = 0;
-        auto fetch_ids = [&]() {
-            while (c_ii < item_hi) {
-                if (c_at != c_ii) {
-                    c_it = p.items[c_ii];
-                    const RequestInfo r = p.reqs[c_it.req];
-                    c_kv_len = r.kv_len;
-                    c_page_begin = r.kv_page_begin;
-                    c_at = c_ii;
-                }
-                if (c_j < c_it.kv_tiles)
-                    break;
-                ++c_ii;
-                c_j = 0;
-            }
-            if (c_ii < item_hi) {
-                const int j0 = prefill_kv_key_at(c_it, c_j, T);
-                for (int t = pt; t < T; t += NP) {
-                    int *dst = &id_ring[(n_ids % kIdRing) * Tr::kIdsPerTile + t];
-                    const int jj = j0 + t;
-                    if (jj < c_kv_len) {
-                        const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
-                        cp_async_4(smem_u32(dst), p.kv_indices + c_page_begin + lp);
-                    } else {
-                        *dst = -1;
-                    }
-                }
-            }
-            cp_async_commit();
-            ++c_j;
-            ++n_ids;
-        };
-        auto sync_producers = [] { asm volatile("bar.sync 1, %0;\n" ::"n"(Tr::kProducers) : "memory"); };
-        for (int k = 0; k < kIdRing - 1; ++k)
-            fetch_ids();
-        uint32_t n = 0;    // K/V ring position
-        uint32_t n_t = 0;  // tiles gathered so far
-        bool okp = true;
-        for (int ii = item_lo; okp && ii < item_hi; ++ii) {
-            const PrefillItem it = p.items[ii];
-            const int n_tiles = it.kv_tiles;
-            if (n_tiles <= 0)
-                continue;
-            for (int j = 0; okp && j < n_tiles; ++j, ++n_t) {
-                const int j0 = prefill_kv_key_at(it, j, T);
-                sync_producers();  // every producer is done with the ring entry refilled next
-                fetch_ids();
-                cp_async_wait<kIdRing - 1>();
-                sync_producers();  // this tile's ids are visible to all producers
-                const int *ids = &id_ring[(n_t % kIdRing) * Tr::kIdsPerTile];
-                const uint32_t full = bar(B::kFull + n % NS);  // K and V of the tile complete it
-                for (int isv = 0; isv < 2; ++isv, ++n) {
-                    const int s = n % NS;
-                    const bool w_ok =
-                        n < NS || mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, p.wait_ns);
-                    okp = bar_red_and(1, NP, w_ok);  // every producer takes the same way out
-                    if (!okp)
-                        break;
-                    const uint16_t *src = isv ? p.v_cache : p.k_cache;
-                    for (int u = pt; u < kUnits; u += NP) {
-                        const int t = u / (CH / 8), pl = u % (CH / 8);  // row, 64-column chunk
-                        const int jj = j0 + t;
-                        const int page = ids[t];
-                        size_t off = 0;
-                        uint32_t bytes = 0;
-                        if (page >= 0) {
-                            if ((unsigned)page < (unsigned)p.num_pages) {
-                                const int lp = p.page_shift >= 0 ? (jj >> p.page_shift) : jj / p.page_size;
-                                const int sl = jj - lp * p.page_size;
-                                off = (((size_t)page * p.page_size + sl) * p.num_kv_heads + it.kv_head) * D + pl * 64;
-                                bytes = 16;
-                            } else {
-                                record_status(p.status, PKV_ERR_DEVICE_BOUNDS);
-                            }
-                        }
-                        const uint32_t line = slot(s) + slot_line(t, pl);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            cp_async_16(line + ((c ^ (t & 7)) << 4), src + off + c * 8, bytes);
-                    }
-                    if (isv == 1)
-                        cp_async_mbar_arrive(full);
-                }
-            }
-        }
-        if (!okp) {
-            record_status(p.status, PKV_ERR_TIMEOUT);
-            abort_flag = 1;
-        }
-        asm volatile("cp.async.wait_all;\n" ::: "memory");
+        gather(threadIdx.x - 9 * 32);
     } else {
         // ------------------------------------------------------------ 8-bit K/V producers
         // Step n: the 8-bit K and V rows of this CTA's n-th KV tile are copied by
