@@ -552,10 +552,11 @@ def extra_workloads(pkv, args, peaks, flush, only=None, oracle=None, cores=None)
         del w
         torch.cuda.empty_cache()
     for W in (wl.LONG_DECODE_WINDOWS if want("long_decode") else ()):
-        w = wl.long_decode(W, device="cuda")
+        w = wl.long_decode(W, device="cuda", batch=args.long_requests)
         plans, runs, bytes_per, step_ms, kern_ms, _ = bench_decode_windows(pkv, w, [W], steps, 2, flush)
         k = kern_ms[0] / steps
-        res[f"long_decode_256x32768_W{W}"] = {
+        key = f"long_decode_{w.batch}x32768_W{W}"
+        res[key] = {
             "gbs": bytes_per[0] / (k * 1e-3) / 1e9, "kernel_ms": k,
             "step_ms": statistics.mean(step_ms), "kv_gb": bytes_per[0] / 1e9,
             "frac_hbm": bytes_per[0] / (k * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -563,7 +564,7 @@ def extra_workloads(pkv, args, peaks, flush, only=None, oracle=None, cores=None)
             "splits": plans[0].info["num_partials"], "ctas": plans[0].info["num_work_items"]}
         del plans, runs
         if oracle is not None:
-            res[f"long_decode_256x32768_W{W}"]["cpu_baseline"] = oracle_decode(oracle, cores, w, n_req=32)
+            res[key]["cpu_baseline"] = oracle_decode(oracle, cores, w, n_req=32)
         del w
         torch.cuda.empty_cache()
     # 8-bit KV caches (E4M3): the batch-decode windows and the long decode. GB/s counts
@@ -673,6 +674,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=EXTRA, default=None,
                     help="run just one of the extra workloads (for profiling) and print its numbers")
+    ap.add_argument("--long-requests", type=int, default=256,
+                    help="requests of the long-context decode workload (256; fewer only for small profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
