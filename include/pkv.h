@@ -129,7 +129,7 @@ typedef struct pkv_plan_desc {
     int32_t disable_split_kv;        /* nonzero: one pass per (request, KV head) */
     int32_t dtype;                   /* pkv_dtype of q, caches and out: PKV_BF16 */
     /* The per-layer arguments flashinfer_backend.py passes with every attention call
-     * (forward_extend / forward_decode: logits_soft_cap = layer.logit_cap, k_scale,
+     * (forward_extend / forward_decode: the layer's logit soft cap, k_scale and
      * v_scale); the pages do not define them further, the readings taken are:
      *   logit_j = cap * tanh(sm_scale * k_scale * q.k_j / cap)   (cap > 0; <= 0: no cap)
      *   out = v_scale * sum_j softmax_j v_j                      (K, V dequantised)
@@ -317,10 +317,10 @@ PKV_API const char *pkv_last_error(void);
 /*
  * pkv_build_kv_indices: build a batch's kv_indptr and kv_indices ON THE DEVICE from a
  * request-to-slot table, so that the page table of a captured plan can be rebuilt
- * between replays without a host round trip (sglang flashinfer_backend.py,
- * call_begin_forward: kv_indptr[1:bs+1] = cumsum(paged_kernel_lens), the
- * create_flashinfer_kv_indices_triton gather from kv_start_idx on, and the
- * sliding-window pool's translate_loc_from_full_to_swa):
+ * between replays without a host round trip (sglang flashinfer_backend.py page,
+ * section call_begin_forward: kv_indptr is the running sum of the kept lengths, each
+ * request's entries come from its table row from its start offset on, and a
+ * sliding-window pool maps them into its own locations):
  *   kv_indptr[0] = 0, kv_indptr[b+1] = kv_indptr[b] + kv_lens[b]
  *   kv_indices[kv_indptr[b] + j] = req_to_token[req_pool_indices[b] * row_stride + kv_start[b] + j]
  *   then, if loc_map != NULL: kv_indices[i] = loc_map[kv_indices[i]]

@@ -1,10 +1,10 @@
 """Oracle of the on-device kv_indices builder (TEST INFRASTRUCTURE: only tests/ may
 import it). Plain Python loops over numpy arrays, shares nothing with the CUDA path.
 
-What it computes (sglang flashinfer_backend.py, call_begin_forward: the
-create_flashinfer_kv_indices_triton call after kv_indptr[1:bs+1] = cumsum of
-paged_kernel_lens; and the sliding-window pool's translate_loc_from_full_to_swa
-applied to the result when the window's KV lives in its own pool):
+What it computes (sglang flashinfer_backend.py page, section call_begin_forward:
+kv_indptr is the running sum of the kept KV lengths, each request's entries are
+read from its row of the request-to-slot table from its start offset on, and when
+the window's KV lives in a pool of its own the entries are mapped into that pool):
 
     kv_indptr[0] = 0, kv_indptr[b+1] = kv_indptr[b] + kv_lens[b]
     kv_indices[kv_indptr[b] + j] = table[req_pool_indices[b], kv_start[b] + j]

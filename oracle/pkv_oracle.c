@@ -12,32 +12,34 @@
  *
  *   for request b, query row i < qo_len_b, query head h:
  *     hk  = h / (H_qo / H_kv)                 consecutive query heads share a KV
- *                                             head ("fuses the head group with the
- *                                             token dimension", flashinfer_backend.py,
- *                                             should_use_tensor_core)
+ *                                             head (the query-head group of a KV
+ *                                             head is packed into the matrix rows:
+ *                                             sglang flashinfer_backend.py page,
+ *                                             section should_use_tensor_core)
  *     p   = q_start_b + i, q_start_b defaulting to kv_len_b - qo_len_b
  *                                             (extend rows sit at prefix + i:
- *                                             flashinfer_backend.py,
- *                                             _build_swa_prefix_custom_mask, q_abs)
+ *                                             sglang flashinfer_backend.py page,
+ *                                             section _build_swa_prefix_custom_mask)
  *     key j in [0, kv_len_b) is visible iff
  *        (!causal || j <= p) && (window_left < 0 || j >= p - window_left)
  *                                             (window_left = W lets the query at p
  *                                             see [p-W, p], W+1 tokens:
  *                                             AMD flashinfer PR #234, "Sliding
  *                                             window" convention; k_abs >= q_abs -
- *                                             window: flashinfer_backend.py,
- *                                             _build_swa_prefix_custom_mask)
+ *                                             window: sglang flashinfer_backend.py page,
+ *                                             section _build_swa_prefix_custom_mask)
  *     K/V row of key j = cache[kv_indices[kv_indptr[b] + j / P], j % P, hk, :]
  *                                             (paged "NHD" layout with kv_indptr,
  *                                             kv_indices, kv_last_page_len:
- *                                             flashinfer_backend.py, fast_prefill_plan
- *                                             and call_begin_forward)
+ *                                             sglang flashinfer_backend.py page,
+ *                                             sections fast_prefill_plan and
+ *                                             call_begin_forward)
  *     s_j = sm_scale * sum_c q[c] k_j[c]
  *     lse = ln sum_{j visible} exp(s_j)        (natural log of the scaled logits)
  *     out = sum_{j visible} exp(s_j - lse) v_j
  *   pkv_oracle_attention_ext adds the three per-layer arguments the pages pass with
  *   every attention call (flashinfer_backend.py forward_extend / forward_decode:
- *   logits_soft_cap = layer.logit_cap, k_scale, v_scale), which the pages do not
+ *   the layer's logit soft cap, k_scale and v_scale), which the pages do not
  *   define further; the readings taken (plainest ones):
  *     s_j = cap * tanh(sm_scale * k_scale * q.k_j / cap)   (cap > 0; else no cap)
  *     out = v_scale * sum_j exp(s_j - lse) v_j           (K and V dequantised by

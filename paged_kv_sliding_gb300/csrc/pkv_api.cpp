@@ -1,11 +1,12 @@
 // Host side of libpkv: argument validation, the plan (work decomposition with the
 // window fixed at plan time), run dispatch and error reporting.
 //
-// The plan follows the shape of the pages' plan/run split (flashinfer_backend.py:
-// fast_prefill_plan builds the schedule from host-known qo/kv layouts with no
-// device-to-host read; call_begin_forward hands kv_indptr / kv_indices /
-// kv_last_page_len to begin_forward) with the change sglang PR #31501 asks for:
-// window_left and causal are given to the plan, and the run cannot override them.
+// The plan follows the shape of the pages' plan/run split (sglang
+// flashinfer_backend.py page: in section fast_prefill_plan the schedule comes from
+// host-known query and KV layouts without a device-to-host read; in section
+// call_begin_forward the plan receives kv_indptr, kv_indices and kv_last_page_len)
+// with the change sglang PR #31501 asks for: window_left and causal are given to the
+// plan, and the run cannot override them.
 #include <algorithm>
 #include <cstdarg>
 #include <cmath>

@@ -1,6 +1,7 @@
 // Split-KV paged decode kernel: one query row per request, the whole query-head
-// group of a KV head against each streamed K/V row (GQA packing, flashinfer_backend.py
-// should_use_tensor_core: the head group is fused into the MMA rows), online softmax
+// group of a KV head against each streamed K/V row (GQA packing: the query-head group
+// forms the MMA rows, as the sglang flashinfer_backend.py page, section
+// should_use_tensor_core, describes for its tensor-core decode), online softmax
 // in fp32, fp32 partial states per split for the merge pass.
 //
 // The plan has already clipped each CTA's key range [j0, j1) to the visible
@@ -666,7 +667,8 @@ __global__ void __launch_bounds__(DecTraits<D, TT, KV, TPW>::kThreads, DecTraits
         if (it.partial >= 0 && p.merge_counters) {
             // Split-KV: the last CTA of this (request, KV head, head block) group to
             // finish merges the group's partial states through their LSE (the
-            // merge_state of flashinfer_backend.py, n-way) and re-arms the counter.
+            // merge_state of the sglang flashinfer_backend.py page, n-way) and re-arms the
+            // counter.
             __shared__ int last_flag;
             asm volatile("bar.sync 1, %0;\n" ::"n"(NT) : "memory");  // this CTA's partials are written
             if (tid == 0) {

@@ -1,8 +1,9 @@
 // On-device builder of kv_indptr / kv_indices from a request-to-slot table, so that
 // a batch's page table can be rebuilt between CUDA-graph replays without a host
-// round trip (sglang flashinfer_backend.py, call_begin_forward: kv_indptr as the
-// running sum of the kept lengths, the create_flashinfer_kv_indices_triton gather
-// from kv_start on, then the sliding-window pool's translate_loc_from_full_to_swa).
+// round trip (sglang flashinfer_backend.py page, section call_begin_forward: kv_indptr
+// is the running sum of the kept lengths, each request's entries are gathered from
+// its row of the table starting at its kv_start, and a sliding-window pool maps them
+// from full-pool locations to its own).
 //
 //   kv_indptr[b+1] = kv_indptr[b] + kv_lens[b]
 //   kv_indices[kv_indptr[b] + j] = table[req_pool_indices[b] * row_stride + kv_start[b] + j]

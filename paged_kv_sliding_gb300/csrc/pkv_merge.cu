@@ -1,7 +1,7 @@
 // LSE merge kernels.
 //
-// merge_state (flashinfer_backend.py, _safe_merge_state; forward_extend merges the
-// ragged extend partial with the paged prefix partial): for two states over
+// merge_state (sglang flashinfer_backend.py page, sections _safe_merge_state and
+// forward_extend, where the ragged extend partial meets the paged prefix partial): for two states over
 // disjoint key sets, s = ln(e^s_a + e^s_b) and v = (e^s_a v_a + e^s_b v_b) / e^s.
 // The split-KV pass generalises it to n partial states of one row.
 //
