@@ -998,8 +998,14 @@ __global__ void __launch_bounds__(384, 1)
         // page's rows (rows_box keys = rows_box / 8 key groups of the group-major slot).
         // A tile's 2 npg boxes (K, then V) are spread over the three warps, whose TMA
         // issue runs in parallel (one thread issues a box about every 100+ cycles).
-        // Every warp walks the same tiles and waits for the same slots; warp 9 sets the
-        // expected bytes and handles the tail tiles' V rows.
+        // The three warps take every ring position in lockstep: each waits for the slot,
+        // then a named barrier among them (which also carries an expired wait, or warp
+        // 9's failed tail landing, to all three), then warp 9 sets the expected bytes
+        // and the boxes go out. A tile's barrier thus completes only after every warp
+        // has seen both of its slots free, so no warp can fall a whole phase behind
+        // the consumer (a parity wait needs that), whether or not it has a box in the
+        // tile (with one box per tile, warp 11 has none). Warp 9 also handles the tail
+        // tiles' V rows.
         static_assert(!TMA_KV || RAGGED || kGM, "paged TMA boxes fill the group-major layout");
         const int pw = warp - 9;  // 0, 1, 2
         {
@@ -1013,6 +1019,7 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t n = 0;       // K/V ring position
             uint32_t n_land = 0;  // tail V tiles so far: the phase of kVLand (warp 9)
             bool okp = true;
+            bool land_ok = true;  // warp 9: the last tail V tile landed
             for (int ii = item_lo; okp && ii < item_hi; ++ii) {
                 const PrefillItem it = p.items[ii];
                 const int n_tiles = it.kv_tiles;
@@ -1052,12 +1059,11 @@ __global__ void __launch_bounds__(384, 1)
                     const uint32_t full = bar(B::kFull + n % NS);
                     for (int isv = 0; isv < 2; ++isv, ++n) {
                         const int s = n % NS;
-                        if (n >= NS) {
-                            okp = __all_sync(0xffffffffu, mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v,
-                                                                    p.wait_ns));
-                            if (!okp)
-                                break;
-                        }
+                        const bool w_ok =
+                            n < NS || mbar_wait(bar(B::kEmpty + s), ((n / NS) - 1) & 1, abort_v, p.wait_ns);
+                        okp = bar_red_and(1, 96, w_ok && land_ok);
+                        if (!okp)
+                            break;
                         const bool vtail = isv == 1 && tail;
                         const uint32_t land = vtail ? bar(B::kVLand) : full;
                         if (pw == 0 && lane == 0) {
@@ -1080,11 +1086,12 @@ __global__ void __launch_bounds__(384, 1)
                         if (isv == 0 && j + 1 < n_tiles)
                             pg_next = load_id(j + 1);
                         if (vtail && pw == 0) {
-                            okp = __all_sync(0xffffffffu,
-                                             mbar_wait(bar(B::kVLand), n_land & 1, abort_v, p.wait_ns));
+                            // (a failed landing reaches the other warps at the next barrier)
+                            land_ok = __all_sync(0xffffffffu,
+                                                 mbar_wait(bar(B::kVLand), n_land & 1, abort_v, p.wait_ns));
                             ++n_land;
-                            if (!okp)
-                                break;
+                            if (!land_ok)
+                                continue;
                             const int vr = max(0, rq.kv_len - j0);
                             const int n16 = (T - vr) * 8;  // 16-byte granules per chunk
                             for (int idx = lane; idx < n16 * NCH; idx += 32) {
@@ -1101,6 +1108,7 @@ __global__ void __launch_bounds__(384, 1)
                     pg = pg_next;
                 }
             }
+            okp = okp && land_ok;
             if (!okp && lane == 0) {
                 record_status(p.status, PKV_ERR_TIMEOUT);
                 abort_flag = 1;
